@@ -1,0 +1,256 @@
+"""Seeded synthetic BEV-pooling workloads.
+
+This module only draws inputs: per-frustum-point BEV cell ids (-1 = dropped),
+depth probabilities and image features.  It holds none of the pooling
+arithmetic (no sort, no map, no scatter-reduce), so both the CUDA path and
+the FP64 oracle consume what it produces without sharing any of the method.
+
+The workloads stand in for the configurations of "Accelerating BEV Pooling
+on NVIDIA GPUs for Physical AI Applications" (section "Classify the memory
+regime": ~209K scatter points, C=80, derived from nuScenes samples; Table 1
+lists further sizes).  nuScenes itself is not used: every workload is drawn
+from a seeded numpy PCG64 generator.
+
+Layouts (shared by both sides):
+  depth  [NC, D, H, W]   (frustum point p = ((nc*D + d)*H + h)*W + w)
+  feat   [NC, H, W, C]   (NHWC, one row of C channels per image pixel)
+  out    [n_cells, C]
+  cell_ids[p] in [0, n_cells) or -1 for a dropped frustum point.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+
+E4M3_MAX = 448.0
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    NC: int
+    D: int
+    H: int
+    W: int
+    C: int
+    n_cells: int
+    cell_ids: np.ndarray          # int32 [NC*D*H*W]
+    depth: np.ndarray             # float16 [NC,D,H,W]  or uint8 E4M3 codes
+    feat: np.ndarray              # float16 [NC,H,W,C]  or uint8 E4M3 codes
+    dtype: str = "f16"            # "f16" or "e4m3"
+    depth_scale: float = 1.0      # E4M3 only: depth value = code * depth_scale
+    feat_scale: float = 1.0       # E4M3 only: feat value = code * feat_scale
+    grid: tuple = ()              # (B, Y, X) of the BEV grid, n_cells = B*Y*X
+    recipe: str = ""
+
+    @property
+    def n_frustum(self) -> int:
+        return self.NC * self.D * self.H * self.W
+
+    @property
+    def n_feat_rows(self) -> int:
+        return self.NC * self.H * self.W
+
+    @property
+    def n_kept(self) -> int:
+        return int(np.count_nonzero(self.cell_ids >= 0))
+
+    def dims(self) -> tuple:
+        return (self.NC, self.D, self.H, self.W)
+
+
+def _softmax_depth(rng: np.random.Generator, NC: int, D: int, H: int, W: int, sigma: float) -> np.ndarray:
+    logits = rng.normal(0.0, sigma, size=(NC, D, H, W))
+    logits -= logits.max(axis=1, keepdims=True)
+    e = np.exp(logits)
+    return (e / e.sum(axis=1, keepdims=True)).astype(np.float16)
+
+
+def _normal_feat(rng: np.random.Generator, NC: int, H: int, W: int, C: int) -> np.ndarray:
+    return rng.standard_normal(size=(NC, H, W, C), dtype=np.float32).astype(np.float16)
+
+
+def quantize_e4m3(x: np.ndarray, scale: float) -> np.ndarray:
+    """E4M3 codes of x/scale, rounded to nearest even by torch's CPU cast."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)) / torch.tensor(scale, dtype=torch.float32)
+    q = t.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).numpy().copy()
+
+
+def tiny(seed: int = 0) -> Workload:
+    """1 camera, D=8, 4x8 feature map, C=8, 16x16 grid; uniform cells; 25% dropped.
+
+    Inputs are drawn in fp32 and handed to both sides as fp16."""
+    NC, D, H, W, C, Y, X = 1, 8, 4, 8, 8, 16, 16
+    rng = np.random.default_rng(seed)
+    feat = _normal_feat(rng, NC, H, W, C)
+    depth = _softmax_depth(rng, NC, D, H, W, 1.0)
+    nf = NC * D * H * W
+    dropped = rng.random(nf) < 0.25
+    cells = rng.integers(0, Y * X, size=nf, dtype=np.int64).astype(np.int32)
+    cells[dropped] = -1
+    return Workload("tiny", NC, D, H, W, C, Y * X, cells, depth, feat, grid=(1, Y, X),
+                    recipe=f"seed {seed}: feat N(0,1); depth softmax over D of N(0,1) logits; "
+                           "cells uniform over 256; Bernoulli(0.25) dropped")
+
+
+def _ring_cells(rng: np.random.Generator, n: int, centre: float, r_in: float, r_span: float,
+                exponent: float, X: int) -> np.ndarray:
+    u = rng.random(n)
+    theta = rng.random(n) * (2.0 * math.pi)
+    r = r_in + r_span * u ** exponent
+    y = np.floor(centre + r * np.sin(theta)).astype(np.int64)
+    x = np.floor(centre + r * np.cos(theta)).astype(np.int64)
+    return (y * X + x).astype(np.int32)
+
+
+RING_EXPONENT = 1.6
+
+
+def canonical(seed: int = 1) -> Workload:
+    """6 cameras, D=118, 32x88 features, C=80, 360x360 grid (1,993,728 frustum points).
+
+    Each frustum point is kept with probability 0.105 (about 209K kept) and
+    lands in a ring of radius 40..150 cells around the grid centre with
+    r = 40 + 110*u**1.6, so cells near the inner edge collect more points and
+    interval lengths are skewed (1 up to about 60)."""
+    NC, D, H, W, C, Y, X = 6, 118, 32, 88, 80, 360, 360
+    rng = np.random.default_rng(seed)
+    feat = _normal_feat(rng, NC, H, W, C)
+    depth = _softmax_depth(rng, NC, D, H, W, 2.0)
+    nf = NC * D * H * W
+    keep = rng.random(nf) < 0.105
+    cells = np.full(nf, -1, dtype=np.int32)
+    cells[keep] = _ring_cells(rng, int(keep.sum()), 180.0, 40.0, 110.0, RING_EXPONENT, X)
+    return Workload("canonical", NC, D, H, W, C, Y * X, cells, depth, feat, grid=(1, Y, X),
+                    recipe=f"seed {seed}: feat N(0,1) fp16; depth softmax over D of N(0,sigma=2) logits; "
+                           f"keep Bernoulli(0.105); ring r=40+110*u^{RING_EXPONENT}, theta~U(0,2pi)")
+
+
+def canonical_fp8(seed: int = 1) -> Workload:
+    """The canonical workload (same cell ids) with feat and depth as E4M3.
+
+    feat_scale = max|feat| / 448 and depth_scale = max(depth), so the depth
+    codes lie in [0, 1]; codes are round-to-nearest-even of value/scale."""
+    wl = canonical(seed)
+    f32 = wl.feat.astype(np.float32)
+    d32 = wl.depth.astype(np.float32)
+    fs = float(np.float32(np.abs(f32).max() / np.float32(E4M3_MAX)))
+    ds = float(np.float32(d32.max()))
+    return dataclasses.replace(
+        wl, name="canonical_fp8", dtype="e4m3",
+        feat=quantize_e4m3(f32, fs).reshape(wl.feat.shape),
+        depth=quantize_e4m3(d32, ds).reshape(wl.depth.shape),
+        feat_scale=fs, depth_scale=ds,
+        recipe=wl.recipe + "; then E4M3 with feat_scale=max|feat|/448, depth_scale=max(depth)")
+
+
+def bevdet(seed: int = 3) -> Workload:
+    """Geometry-derived map: 6 pinhole cameras at the ego origin, yaw k*60 deg.
+
+    fx = fy = 800, image 704x256 with the principal point at its centre,
+    16x downsampled to a 16x44 feature map (pixel centre ((w+0.5)*16,
+    (h+0.5)*16)), D = 59 depth bins at z = 1..59 m along the optical axis.
+    Ego X is forward of camera 0, Y left, Z up.  Cells are 0.8 m over
+    +-51.2 m (128x128), cell = iy*128 + ix; points off the grid or with
+    Z outside [-5, 3] m are dropped.  C = 64, feat N(0,1), depth softmax of
+    N(0,1) logits."""
+    NC, D, H, W, C, Y, X = 6, 59, 16, 44, 64, 128, 128
+    rng = np.random.default_rng(seed)
+    feat = _normal_feat(rng, NC, H, W, C)
+    depth = _softmax_depth(rng, NC, D, H, W, 1.0)
+    fx = fy = 800.0
+    cx, cy = 352.0, 128.0
+    z = np.arange(1, D + 1, dtype=np.float64)[:, None, None]            # [D,1,1]
+    v = ((np.arange(H, dtype=np.float64) + 0.5) * 16.0)[None, :, None]   # [1,H,1]
+    u = ((np.arange(W, dtype=np.float64) + 0.5) * 16.0)[None, None, :]   # [1,1,W]
+    x_cam = (u - cx) / fx * z
+    y_cam = (v - cy) / fy * z
+    cells = np.empty((NC, D, H, W), dtype=np.int32)
+    for k in range(NC):
+        yaw = math.radians(60.0 * k)
+        # forward axis (cos, sin, 0); image-right axis (sin, -cos, 0); image-down axis (0, 0, -1)
+        ex = z * math.cos(yaw) + x_cam * math.sin(yaw)
+        ey = z * math.sin(yaw) - x_cam * math.cos(yaw)
+        ez = -y_cam + 0.0 * ex
+        ix = np.floor((ex + 51.2) / 0.8).astype(np.int64)
+        iy = np.floor((ey + 51.2) / 0.8).astype(np.int64)
+        ok = (ix >= 0) & (ix < X) & (iy >= 0) & (iy < Y) & (ez >= -5.0) & (ez <= 3.0)
+        c = np.where(ok, iy * X + ix, -1)
+        cells[k] = np.broadcast_to(c, (D, H, W)).astype(np.int32)
+    return Workload("bevdet", NC, D, H, W, C, Y * X, cells.reshape(-1), depth, feat, grid=(1, Y, X),
+                    recipe=f"seed {seed}: pinhole geometry (fx=fy=800, 704x256 image, /16, yaw k*60deg, "
+                           "z=1..59 m), 0.8 m cells over +-51.2 m, Z in [-5,3] m")
+
+
+def dram_batch(seeds: tuple = (10, 11, 12, 13), keep: float = 0.2759) -> Workload:
+    """Four canonical frusta (24 cameras) into a batched [4, 512, 512] grid, C=128.
+
+    Per sample: feat N(0,1) fp16, depth softmax of N(0,2) logits, keep
+    Bernoulli(0.2759) (about 2.2M kept in total), cells uniform in the disc
+    of radius 250 around (256, 256): r = 250*sqrt(u), theta ~ U(0, 2pi).
+    Sample b's cells are offset by b*512*512."""
+    D, H, W, C, Y, X = 118, 32, 88, 128, 512, 512
+    cams = 6
+    feats, depths, cell_parts = [], [], []
+    for b, seed in enumerate(seeds):
+        rng = np.random.default_rng(seed)
+        feats.append(_normal_feat(rng, cams, H, W, C))
+        depths.append(_softmax_depth(rng, cams, D, H, W, 2.0))
+        nf = cams * D * H * W
+        kept = rng.random(nf) < keep
+        n = int(kept.sum())
+        u = rng.random(n)
+        theta = rng.random(n) * (2.0 * math.pi)
+        r = 250.0 * np.sqrt(u)
+        y = np.floor(256.0 + r * np.sin(theta)).astype(np.int64)
+        x = np.floor(256.0 + r * np.cos(theta)).astype(np.int64)
+        c = np.full(nf, -1, dtype=np.int32)
+        c[kept] = (b * Y * X + y * X + x).astype(np.int32)
+        cell_parts.append(c)
+    NC = cams * len(seeds)
+    return Workload("dram_batch", NC, D, H, W, C, len(seeds) * Y * X, np.concatenate(cell_parts),
+                    np.concatenate(depths, axis=0), np.concatenate(feats, axis=0), grid=(len(seeds), Y, X),
+                    recipe=f"seeds {list(seeds)}: per sample feat N(0,1), depth softmax N(0,2) logits, "
+                           f"keep Bernoulli({keep}), cells uniform in disc r<=250 of a 512x512 grid")
+
+
+def custom(NC: int, D: int, H: int, W: int, C: int, n_cells: int, cell_ids: np.ndarray,
+           seed: int = 0, dtype: str = "f16", name: str = "custom",
+           depth: Optional[np.ndarray] = None, feat: Optional[np.ndarray] = None) -> Workload:
+    """A workload with caller-chosen cell ids (edge cases); random depth/feat unless given."""
+    rng = np.random.default_rng(seed)
+    if feat is None:
+        feat = _normal_feat(rng, NC, H, W, C)
+    if depth is None:
+        depth = _softmax_depth(rng, NC, D, H, W, 1.0)
+    wl = Workload(name, NC, D, H, W, C, n_cells, np.ascontiguousarray(cell_ids, dtype=np.int32).reshape(-1),
+                  np.ascontiguousarray(depth, dtype=np.float16), np.ascontiguousarray(feat, dtype=np.float16),
+                  grid=(1, 1, n_cells), recipe=f"custom seed {seed}")
+    if dtype == "e4m3":
+        f32 = wl.feat.astype(np.float32)
+        d32 = wl.depth.astype(np.float32)
+        fs = float(np.float32(max(np.abs(f32).max(), 1e-30) / np.float32(E4M3_MAX)))
+        ds = float(np.float32(max(d32.max(), 1e-30)))
+        wl = dataclasses.replace(wl, dtype="e4m3", feat=quantize_e4m3(f32, fs).reshape(wl.feat.shape),
+                                 depth=quantize_e4m3(d32, ds).reshape(wl.depth.shape),
+                                 feat_scale=fs, depth_scale=ds)
+    return wl
+
+
+CONFIGS = {
+    "tiny": tiny,
+    "canonical": canonical,
+    "canonical_fp8": canonical_fp8,
+    "bevdet": bevdet,
+    "dram_batch": dram_batch,
+}
+
+
+def make(name: str) -> Workload:
+    return CONFIGS[name]()
