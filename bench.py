@@ -1,0 +1,399 @@
+"""Benchmark of the BEV-pooling hot path on one GB300 (or N independent replicas).
+
+A step is one pass of the whole hot path over one synthetic frame:
+bevpool_build_map (compaction, stable radix sort, index derivation,
+intervals) followed by bevpool_forward (interval-owned scatter-reduce).  L2 is
+flushed (a 256 MiB buffer is written) before the map build and again before
+the forward, so both run from HBM; each is bracketed by CUDA events on the
+stream it is launched on.  The headline value is the forward's device time in
+microseconds per call (lower is better); the map build and the whole step are
+reported beside it.
+
+Also reported, on one line of JSON:
+  roofline      the forward kernel's algorithmic bytes / event time against
+                the measured HBM copy bandwidth;
+  e2e           the same forward driven from pinned host buffers through the
+                C ABI (H2D of depth+feat, forward, D2H of the output);
+  cpu_baseline  the FP64 oracle (single thread) on the same workload;
+  extra         map-build time, warm-L2 CUDA-graph replay of the forward
+                (the timing method of the pages' Table 1), L2-level gather GB/s.
+
+--impl reference times the oracle alone (the reference arm of this build).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "BEV-pool forward µs/call and GB/s vs L2/HBM roofline (209K pts, C=80, FP16/FP8)"
+FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+FORWARD_SOURCES = ["forward_impl.cuh", "forward_f16.cu", "forward_e4m3.cu", "bevpool_internal.cuh"]
+
+
+def forward_source_hash() -> str:
+    h = hashlib.sha1()
+    for f in FORWARD_SOURCES:
+        with open(os.path.join(ROOT, "depth_weighted_scatter_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> tuple:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per forward launch from a committed ncu capture, if it was
+    taken on the current forward source."""
+    p = os.path.join(ROOT, "profiles", "forward_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("source_hash") == forward_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def bytes_model(wl, n_points: int, n_intervals: int) -> dict:
+    """Bytes one forward must move.  'footprint' = every array the forward
+    touches, once (the compulsory HBM traffic after an L2 flush);
+    'gather' = what the owners actually read per point (L2-level)."""
+    eb = 2 if wl.dtype == "f16" else 1
+    idx = 12 * n_points                  # ranks_depth, ranks_feat, ranks_bev
+    iv = 8 * n_intervals                 # interval_starts, interval_lengths
+    depth = wl.n_frustum * eb
+    feat = wl.n_feat_rows * wl.C * eb
+    out = wl.n_cells * wl.C * 2
+    footprint = idx + iv + depth + feat + out
+    gather = idx + iv + n_points * eb + n_points * wl.C * eb + out
+    return dict(index=idx, intervals=iv, depth=depth, feat=feat, out=out, footprint=footprint, gather=gather)
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled while it runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu_index = gpu_index
+        self.period_ms = period_ms
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu_index), "-lms", str(self.period_ms)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(values, world: int, device):
+    """Element-wise max of a list of floats over all ranks."""
+    if world == 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def cpu_oracle_time(wl, budget_s: float = 10.0, max_reps: int = 50) -> dict:
+    """Times the oracle's forward on the full workload, single-threaded."""
+    import oracle
+
+    oracle.build()
+    oracle.forward(wl.dtype, wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat,
+                   wl.depth_scale, wl.feat_scale)       # load + page in
+    times = []
+    t_start = time.perf_counter()
+    while len(times) < max_reps and (time.perf_counter() - t_start < budget_s or len(times) < 3):
+        t0 = time.perf_counter()
+        oracle.forward(wl.dtype, wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat,
+                       wl.depth_scale, wl.feat_scale)
+        times.append(time.perf_counter() - t0)
+    return {"value": statistics.mean(times) * 1e6, "unit": "us/call", "cores": 1, "kind": "oracle",
+            "sample": f"full {wl.name} workload ({wl.n_kept} points, C={wl.C}), {len(times)} calls of the "
+                      f"single-threaded FP64 C oracle forward; host has {os.cpu_count()} cores"}
+
+
+def run_reference(args) -> None:
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from depth_weighted_scatter_gb300 import workloads
+    import oracle
+
+    wl = workloads.make(args.config)
+    oracle.build()
+    call = lambda: oracle.forward(wl.dtype, wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat,
+                                  wl.depth_scale, wl.feat_scale)
+    for _ in range(args.warmup):
+        call()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        call()
+        times.append(time.perf_counter() - t0)
+    v = statistics.mean(times) * 1e6
+    line = {"metric": METRIC, "value": v, "unit": "us/call", "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "points": wl.n_kept, "C": wl.C, "n_cells": wl.n_cells},
+            "cpu_baseline": {"value": v, "unit": "us/call", "cores": 1, "kind": "oracle",
+                             "sample": f"each step one full {wl.name} forward of the single-threaded FP64 C oracle"},
+            "e2e": {"value": v, "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args) -> None:
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+
+    from depth_weighted_scatter_gb300 import bevpool, workloads
+
+    wl = workloads.make(args.config)
+    dt = bevpool.BEVPOOL_F16 if wl.dtype == "f16" else bevpool.BEVPOOL_E4M3
+    view = np.uint16 if dt == bevpool.BEVPOOL_F16 else np.uint8
+    depth_h = torch.from_numpy(np.ascontiguousarray(wl.depth).reshape(-1).view(view).copy()).pin_memory()
+    feat_h = torch.from_numpy(np.ascontiguousarray(wl.feat).reshape(-1).view(view).copy()).pin_memory()
+    cells = torch.from_numpy(wl.cell_ids).to(device)
+    depth = depth_h.to(device)
+    feat = feat_h.to(device)
+
+    ws = bevpool.workspace_for(*wl.dims(), wl.n_cells, device)
+    m = bevpool.ScatterMap.allocate(*wl.dims(), wl.n_cells, device)
+    bevpool.build_map(cells, *wl.dims(), wl.n_cells, out=m, workspace=ws, sync=True)
+    n_pts, n_int = m.n_points, m.n_intervals
+    cap = (n_pts, n_int)
+    out = torch.empty((wl.n_cells, wl.C), dtype=torch.float16, device=device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def fwd(o=out):
+        bevpool.forward(m, depth, feat, wl.C, dtype=dt, depth_scale=wl.depth_scale, feat_scale=wl.feat_scale,
+                        out=o, capacity=cap)
+
+    def build():
+        bevpool.build_map(cells, *wl.dims(), wl.n_cells, out=m, workspace=ws, sync=False)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        build()
+        flush.zero_()
+        fwd()
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = bevpool.bevpool_kernel_launches()
+    torch.cuda._sleep(20_000_000)            # let the host queue steps ahead of the GPU (outside every event pair)
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        build()
+        ev[i][1].record(stream)
+        flush.zero_()
+        ev[i][2].record(stream)
+        fwd()
+        ev[i][3].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = bevpool.bevpool_kernel_launches() - launches0
+    clocks = sampler.stop()
+
+    build_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    fwd_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps)]
+    fwd_mean, build_mean = statistics.mean(fwd_ms), statistics.mean(build_ms)
+    fwd_mean, build_mean = max_over_ranks([fwd_mean, build_mean], world, device)
+
+    # Correctness guard: the timed map must be the one built up front.
+    counts = m.d_counts.cpu().tolist()
+    if counts[0] != n_pts or counts[1] != n_int:
+        raise RuntimeError(f"map counts changed during timing: {counts} vs {(n_pts, n_int)}")
+
+    # Warm-L2 CUDA-graph replay of the forward (the pages' Table 1 method).
+    warm_us = None
+    try:
+        g_stream = torch.cuda.Stream()
+        g_stream.wait_stream(stream)
+        with torch.cuda.stream(g_stream):
+            for _ in range(3):
+                fwd()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=g_stream):
+                for _ in range(100):
+                    fwd()
+        stream.wait_stream(g_stream)
+        torch.cuda.synchronize()
+        reps = []
+        for _ in range(10):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            reps.append(a.elapsed_time(b) * 1e3 / 100)
+        warm_us = statistics.median(reps)
+    except Exception as e:  # graph capture is an extra, never the headline
+        warm_us = f"unavailable: {type(e).__name__}"
+
+    # End to end through the C ABI from pinned host buffers.
+    out_h = torch.empty((wl.n_cells, wl.C), dtype=torch.float16).pin_memory()
+    e2e_steps = min(args.steps, 200)
+    e2e_ms = []
+    for i in range(e2e_steps + 3):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        depth.copy_(depth_h, non_blocking=True)
+        feat.copy_(feat_h, non_blocking=True)
+        fwd()
+        out_h.copy_(out, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_us = max_over_ranks([statistics.mean(e2e_ms) * 1e3], world, device)[0]
+    h2d = depth_h.numel() * depth_h.element_size() + feat_h.numel() * feat_h.element_size()
+    d2h = out_h.numel() * out_h.element_size()
+
+    if rank != 0:
+        return
+    bm = bytes_model(wl, n_pts, n_int)
+    peak, peak_kind = measured_peaks()
+    fwd_s = fwd_mean / 1e3
+    achieved = bm["footprint"] / fwd_s / 1e9
+    line = {
+        "metric": METRIC,
+        "value": fwd_mean * 1e3,
+        "unit": "us/call",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": build_mean + fwd_mean,
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.dtype,
+        "data": "synthetic (seeded generator shaped like the pages' workload; nuScenes not used)",
+        "config": {"workload": f"{wl.name}: NC={wl.NC} D={wl.D} H={wl.H} W={wl.W} C={wl.C} grid={wl.grid} "
+                               f"points={n_pts} intervals={n_int}",
+                   "l2": "flushed (256 MiB written) before the map build and before the forward",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic(wl.name),
+                     "kernel": "k_forward", "bytes_per_launch": bm["footprint"],
+                     "peak_source": f"hbm_gbs of MEASURED_PEAKS.json ({peak_kind})"},
+        "cpu_baseline": cpu_oracle_time(wl) if (world == 1 and not args.no_cpu_baseline) else None,
+        "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "extra": {
+            "forward_us_median": statistics.median(fwd_ms) * 1e3,
+            "build_map_us": build_mean * 1e3,
+            "forward_us_warm_l2_graph": warm_us,
+            "gather_bytes": bm["gather"],
+            "gather_gbs_cold": bm["gather"] / fwd_s / 1e9,
+            "gather_gbs_warm": (bm["gather"] / (warm_us * 1e-6) / 1e9) if isinstance(warm_us, float) else None,
+            "bytes_model": bm,
+            "forward_source_hash": forward_source_hash(),
+            "pages_context_us": {"v3_fp16_rtx_pro_6000": 17.3, "v3_fp8_rtx_pro_6000": 16.4,
+                                 "v2_fp16_rtx_pro_6000": 274.0, "v3_fp16_a6000_dram_tuned": 90.0},
+        },
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="canonical",
+                    choices=["tiny", "canonical", "canonical_fp8", "bevdet", "dram_batch"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        if args.steps > 100:
+            args.steps = 10             # each reference step is a full CPU forward (~0.5 s)
+        args.warmup = min(args.warmup, 3)
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

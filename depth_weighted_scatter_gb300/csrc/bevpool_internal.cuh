@@ -1,0 +1,140 @@
+// bevpool_internal.cuh -- shared device helpers and host-side launch plumbing
+// for libbevpool (sm_103a).  Not part of the public ABI (include/bevpool.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "../../include/bevpool.h"
+
+namespace bevpool {
+
+constexpr int kThreads = 256;            // every kernel in the library runs 256-thread CTAs
+constexpr int kWarps = kThreads / 32;
+
+// Launch accounting: every kernel launch made by the library bumps this.
+extern std::atomic<int64_t> g_kernel_launches;
+
+inline void count_launch() { g_kernel_launches.fetch_add(1, std::memory_order_relaxed); }
+
+// Per-device properties the host code needs (cached).
+struct DeviceInfo {
+    int sm_count = 0;
+    int l2_bytes = 0;
+    int max_smem_optin = 0;
+};
+bool device_info(DeviceInfo *out);
+
+inline int64_t div_up(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- device helpers
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Exclusive sum over the 256 threads of a CTA.  `scratch` needs kWarps+1 ints.
+// Returns this thread's exclusive prefix; *total receives the CTA sum.
+__device__ __forceinline__ int cta_exclusive_sum(int v, int *scratch, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scratch[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < kWarps ? scratch[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < kWarps; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < kWarps) scratch[lane] = w;   // inclusive warp totals
+    }
+    __syncthreads();
+    int warp_excl = warp ? scratch[warp - 1] : 0;
+    int tot = scratch[kWarps - 1];
+    __syncthreads();                            // scratch may be reused right after
+    *total = tot;
+    return warp_excl + x - v;
+}
+
+// Sum over the CTA (result valid in every thread).  `scratch` needs kWarps ints.
+__device__ __forceinline__ long long cta_sum_ll(long long v, long long *scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    long long t = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) t += scratch[w];
+    __syncthreads();
+    return t;
+}
+
+// Max over the CTA (result valid in every thread).  `scratch` needs kWarps ints.
+__device__ __forceinline__ int cta_max(int v, int *scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    int t = scratch[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) t = max(t, scratch[w]);
+    __syncthreads();
+    return t;
+}
+
+// ---------------------------------------------------------------- launchers
+
+// Build-map pipeline (build_map.cu).  All pointers device; sizes validated.
+struct BuildMapArgs {
+    const int32_t *cell_ids;
+    int32_t NC, D, H, W, n_cells;
+    int32_t *ranks_depth, *ranks_feat, *ranks_bev;
+    int32_t *interval_starts, *interval_lengths;
+    int32_t *d_counts;
+    void *workspace;
+    size_t workspace_bytes;
+    cudaStream_t stream;
+};
+size_t build_map_workspace_bytes(int64_t n_frustum, int32_t n_cells);
+cudaError_t launch_build_map(const BuildMapArgs &a);
+
+// Forward (forward_f16.cu / forward_e4m3.cu).
+struct ForwardArgs {
+    const void *depth, *feat;
+    const int32_t *ranks_depth, *ranks_feat, *ranks_bev;
+    const int32_t *interval_starts, *interval_lengths;
+    const int32_t *d_counts;
+    int32_t n_points, n_intervals, n_cells, C;
+    int64_t n_depth;          // NC*D*H*W
+    int32_t n_feat_rows;      // NC*H*W
+    float scale;              // depth_scale * feat_scale
+    int streaming_stores;     // 1: evict-first output stores (HBM regime)
+    void *out;
+    cudaStream_t stream;
+};
+bool forward_supported(int dtype, int C);
+cudaError_t launch_forward_f16(const ForwardArgs &a);
+cudaError_t launch_forward_e4m3(const ForwardArgs &a);
+
+// Map validation (abi.cu).
+cudaError_t launch_validate_map(const int32_t *ranks_depth, const int32_t *ranks_feat,
+                                const int32_t *ranks_bev, const int32_t *starts,
+                                const int32_t *lengths, int32_t n_points, int32_t n_intervals,
+                                int64_t n_depth, int32_t n_feat_rows, int32_t n_cells,
+                                int32_t *d_result, cudaStream_t stream);
+
+}  // namespace bevpool

@@ -1,0 +1,200 @@
+/*
+ * bevpool.h -- C ABI of libbevpool, GB300 (sm_103a) BEV pooling.
+ *
+ * BEV pooling is the depth-weighted scatter-reduce of "Accelerating BEV
+ * Pooling on NVIDIA GPUs for Physical AI Applications" (NVIDIA technical
+ * blog), section "Eliminate redundant scatter traffic":
+ *
+ *     out[ranks_bev[t], c] += depth[ranks_depth[t]] * feat[ranks_feat[t], c]
+ *
+ * over every scatter point t of a five-array INT32 scatter map
+ * (ranks_depth, ranks_feat, ranks_bev, interval_starts, interval_lengths).
+ * The map is prepared ahead of the forward (section "Implement
+ * interval-owned scatter-reduce"); each interval is the run of points that
+ * share one BEV cell and is reduced by one owner that writes the cell once.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers marked "device" must point to device memory of the current
+ *     CUDA device; pointers marked "host" to host memory.  The library
+ *     allocates nothing: the caller owns every buffer, including scratch
+ *     ("workspace"), which it sizes with the matching *_workspace_size call.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call only enqueues work on it and returns, except
+ *     where a host output pointer is given: then the call synchronises the
+ *     stream before returning.
+ *   - Errors are returned as bevpool_status; the library never aborts,
+ *     traps or prints.  Arguments are checked on the host before any work
+ *     is enqueued; on an error nothing is enqueued.  A CUDA launch error is
+ *     returned as BEVPOOL_ERR_CUDA and cleared from the runtime's
+ *     last-error slot.
+ *   - Layouts (frustum point index p = ((nc*D + d)*H + h)*W + w):
+ *       cell_ids [NC*D*H*W] int32, -1 = point dropped, else in [0, n_cells)
+ *       depth    [NC, D, H, W]  (element p belongs to frustum point p)
+ *       feat     [NC, H, W, C]  (row r = (nc*H + h)*W + w holds C channels)
+ *       out      [n_cells, C]   fp16 (IEEE binary16), row-major
+ *   - Sizes: NC*D*H*W < 2^31, n_cells*C < 2^31.
+ *   - Calls on different streams may run concurrently only if they share no
+ *     output or workspace buffer.
+ */
+#ifndef BEVPOOL_H
+#define BEVPOOL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BEVPOOL_API __attribute__((visibility("default")))
+#else
+#define BEVPOOL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bevpool_status {
+    BEVPOOL_OK = 0,
+    BEVPOOL_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad alignment      */
+    BEVPOOL_ERR_OUT_OF_RANGE = 2,  /* a cell id or map entry outside its range   */
+    BEVPOOL_ERR_UNSUPPORTED = 3,   /* channel count / dtype with no kernel       */
+    BEVPOOL_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required */
+    BEVPOOL_ERR_CUDA = 5           /* a CUDA runtime call or launch failed       */
+} bevpool_status;
+
+typedef enum bevpool_dtype {
+    BEVPOOL_F16 = 0,   /* depth and feat are IEEE binary16                         */
+    BEVPOOL_E4M3 = 1   /* depth and feat are OCP FP8 E4M3 codes, one scale each    */
+} bevpool_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+BEVPOOL_API const char *bevpool_status_string(bevpool_status status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+BEVPOOL_API int32_t bevpool_version(void);
+
+/* Number of kernels this library has launched in this process so far
+ * (all devices, all streams).  Used to count launches in a timed region. */
+BEVPOOL_API int64_t bevpool_kernel_launches(void);
+
+/* Whether channel count C has a compiled forward kernel for dtype (1 / 0). */
+BEVPOOL_API int32_t bevpool_forward_supported(bevpool_dtype dtype, int32_t C);
+
+/*
+ * Bytes of device workspace bevpool_build_map needs for a frustum of
+ * n_frustum = NC*D*H*W points and a grid of n_cells cells.  Returns 0 for
+ * invalid sizes.
+ */
+BEVPOOL_API size_t bevpool_build_map_workspace_size(int64_t n_frustum, int32_t n_cells);
+
+/*
+ * Build the five-array scatter map from per-frustum-point BEV cell ids
+ * (the map the section "Implement interval-owned scatter-reduce" says is
+ * prepared ahead).  Bit-exact and deterministic: the kept points are sorted
+ * by (cell, p) -- a stable sort of frustum order by cell -- and
+ *     ranks_bev[t]   = cell of the t-th sorted point
+ *     ranks_depth[t] = its frustum index p
+ *     ranks_feat[t]  = nc*H*W + h*W + w   (the only integer division, done here)
+ * Intervals are the maximal runs of equal ranks_bev, in ascending cell order:
+ *     interval_starts[i], interval_lengths[i] (>= 1), contiguous, summing to n.
+ *
+ *   cell_ids          device, [NC*D*H*W] int32; -1 drops the point.
+ *   NC, D, H, W       frustum dimensions (all >= 1).
+ *   n_cells           number of BEV cells (>= 1).
+ *   ranks_*           device, capacity NC*D*H*W int32 each (n entries written).
+ *   interval_*        device, capacity min(NC*D*H*W, n_cells) int32 each.
+ *   d_counts          device, int32[3]: {n_points, n_intervals, n_invalid},
+ *                     written by the enqueued work.  n_invalid counts ids
+ *                     that are neither -1 nor in [0, n_cells); such points are
+ *                     treated as dropped.
+ *   h_counts          host, int32[3] or NULL.  If non-NULL the call copies
+ *                     d_counts here, synchronises `stream`, and returns
+ *                     BEVPOOL_ERR_OUT_OF_RANGE when n_invalid > 0.
+ *   workspace         device scratch of at least
+ *                     bevpool_build_map_workspace_size(NC*D*H*W, n_cells)
+ *                     bytes, 256-byte aligned; contents need no initialisation
+ *                     and are clobbered.
+ */
+BEVPOOL_API bevpool_status bevpool_build_map(const int32_t *cell_ids, int32_t NC, int32_t D, int32_t H,
+                                 int32_t W, int32_t n_cells, int32_t *ranks_depth,
+                                 int32_t *ranks_feat, int32_t *ranks_bev,
+                                 int32_t *interval_starts, int32_t *interval_lengths,
+                                 int32_t *d_counts, int32_t *h_counts, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/*
+ * Interval-owned forward (sections "Eliminate redundant scatter traffic"
+ * and "Implement interval-owned scatter-reduce"): for every interval i,
+ *     out[ranks_bev[s], c] = scale * sum_{t in [s, s+len)}
+ *                            depth[ranks_depth[t]] * feat[ranks_feat[t], c]
+ * with s = interval_starts[i], len = interval_lengths[i] and
+ * scale = depth_scale * feat_scale, accumulated in FP32 and rounded once to
+ * fp16 (round to nearest even).  Every one of the n_cells rows of `out` is
+ * written exactly once; rows no interval names are written as zeros.  No
+ * atomics: the result is bit-identical from run to run.
+ *
+ *   dtype             BEVPOOL_F16 or BEVPOOL_E4M3 (depth and feat alike).
+ *   depth             device, [NC, D, H, W] elements of dtype.
+ *   feat              device, [NC*H*W, C] elements of dtype, 16-byte aligned.
+ *   NC, D, H, W       frustum dimensions; bound the indices in the map.
+ *   C                 channels; bevpool_forward_supported(dtype, C) must be 1.
+ *   depth_scale,
+ *   feat_scale        multipliers of the E4M3 code values (use 1 for F16).
+ *   ranks_depth,
+ *   ranks_feat,
+ *   ranks_bev         device, [n_points] int32 (as built by bevpool_build_map).
+ *   interval_starts,
+ *   interval_lengths  device, [n_intervals] int32.
+ *   n_points,
+ *   n_intervals       host counts.  If d_counts is non-NULL they are
+ *                     capacities instead and the counts are read on the
+ *                     device from d_counts[0] and d_counts[1] (clamped to the
+ *                     capacities), so a forward can follow bevpool_build_map
+ *                     on the same stream without a host synchronisation.
+ *   d_counts          device int32[>=2] or NULL.
+ *   n_cells           rows of out.
+ *   out               device, [n_cells, C] fp16, 16-byte aligned; fully
+ *                     overwritten.
+ *
+ * The map is trusted for its ordering (intervals in ascending cell order,
+ * one interval per cell).  Indices are still bounds-checked on the device:
+ * a point whose ranks_depth / ranks_feat lies outside the tensors
+ * contributes nothing, and an interval whose cell lies outside [0, n_cells)
+ * or whose range lies outside [0, n_points) is skipped.  Use
+ * bevpool_validate_map to check a map.
+ */
+BEVPOOL_API bevpool_status bevpool_forward(bevpool_dtype dtype, const void *depth, const void *feat,
+                               int32_t NC, int32_t D, int32_t H, int32_t W, int32_t C,
+                               float depth_scale, float feat_scale, const int32_t *ranks_depth,
+                               const int32_t *ranks_feat, const int32_t *ranks_bev,
+                               const int32_t *interval_starts, const int32_t *interval_lengths,
+                               int32_t n_points, int32_t n_intervals, const int32_t *d_counts,
+                               int32_t n_cells, void *out, void *stream);
+
+/*
+ * Check a scatter map on the device (debug aid; the five-array map of the
+ * section "Eliminate redundant scatter traffic" with the interval structure
+ * of the section "Implement interval-owned scatter-reduce").  Writes to
+ * d_result (device int32[1]) a bit set of the violations found, 0 if none:
+ *     1  interval_starts[0] != 0 or starts not contiguous (start[i+1] != start[i]+len[i])
+ *     2  an interval length < 1, or the lengths do not sum to n_points
+ *     4  ranks_bev differs inside an interval, or interval cells not strictly
+ *        increasing
+ *     8  a ranks_bev entry outside [0, n_cells)
+ *    16  a ranks_depth entry outside [0, NC*D*H*W)
+ *    32  a ranks_feat entry outside [0, NC*H*W)
+ * h_result: host int32[1] or NULL; if non-NULL the call synchronises the
+ * stream, copies the bit set there and returns BEVPOOL_ERR_OUT_OF_RANGE when
+ * it is non-zero.  n_points / n_intervals are host counts.
+ */
+BEVPOOL_API bevpool_status bevpool_validate_map(const int32_t *ranks_depth, const int32_t *ranks_feat,
+                                    const int32_t *ranks_bev, const int32_t *interval_starts,
+                                    const int32_t *interval_lengths, int32_t n_points,
+                                    int32_t n_intervals, int32_t NC, int32_t D, int32_t H,
+                                    int32_t W, int32_t n_cells, int32_t *d_result,
+                                    int32_t *h_result, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BEVPOOL_H */

@@ -1,0 +1,219 @@
+"""GPU parity: libbevpool (through the C ABI) against the FP64 oracle.
+
+Scatter maps must match bit-exactly; forward outputs within the fp16 / E4M3
+tolerances of tests/gpu_common.py.  Every workload below is seeded; the full
+configurations run at their full sizes in the launch configuration the
+benchmark times."""
+import numpy as np
+import pytest
+
+from gpu_common import MAP_KEYS, assert_forward_close, gpu_forward, oracle_forward, upload
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def bp():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from depth_weighted_scatter_gb300 import bevpool
+
+    return bevpool
+
+
+def _gpu_map(bp, wl, cells, sync=True):
+    return bp.build_map(cells, *wl.dims(), wl.n_cells, sync=sync)
+
+
+def _check_map(bp, wl, m):
+    import oracle
+
+    ref = oracle.build_map(wl.cell_ids, *wl.dims(), wl.n_cells)
+    got = m.host()
+    assert got["n_points"] == ref["n_points"] and got["n_intervals"] == ref["n_intervals"]
+    for k in MAP_KEYS:
+        assert np.array_equal(got[k], ref[k]), f"{wl.name}: {k} differs"
+    assert bp.validate_map(m) == 0
+    return ref
+
+
+CONFIGS = ["tiny", "canonical", "canonical_fp8", "bevdet", "dram_batch"]
+
+
+@pytest.mark.parametrize("name", CONFIGS)
+def test_full_config_parity(bp, name, wl_cache):
+    wl = wl_cache(name)
+    cells, depth, feat = upload(wl)
+    m = _gpu_map(bp, wl, cells)
+    _check_map(bp, wl, m)
+    out = torch.full((wl.n_cells, wl.C), float("nan"), dtype=torch.float16, device="cuda")
+    gpu_forward(wl, m, depth, feat, out=out)
+    torch.cuda.synchronize()
+    assert_forward_close(wl, out, oracle_forward(wl))
+
+
+@pytest.mark.parametrize("name", ["canonical", "bevdet"])
+def test_forward_is_deterministic(bp, name, wl_cache):
+    wl = wl_cache(name)
+    cells, depth, feat = upload(wl)
+    m = _gpu_map(bp, wl, cells)
+    a = gpu_forward(wl, m, depth, feat)
+    b = gpu_forward(wl, m, depth, feat)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_device_counts_path_matches_host_counts(bp, wl_cache):
+    """build_map without a host sync, forward reading the counts on the device."""
+    wl = wl_cache("canonical")
+    cells, depth, feat = upload(wl)
+    m_sync = _gpu_map(bp, wl, cells)
+    m_async = _gpu_map(bp, wl, cells, sync=False)
+    a = gpu_forward(wl, m_sync, depth, feat)
+    b = gpu_forward(wl, m_async, depth, feat, capacity=(m_sync.n_points + 1000, m_sync.n_intervals + 500))
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_forward_on_oracle_map(bp, wl_cache):
+    """The forward alone, fed the oracle's map (independent of the GPU map builder)."""
+    import oracle
+
+    wl = wl_cache("bevdet")
+    cells, depth, feat = upload(wl)
+    ref_map = oracle.build_map(wl.cell_ids, *wl.dims(), wl.n_cells)
+    m = bp.ScatterMap.allocate(*wl.dims(), wl.n_cells)
+    for k in MAP_KEYS:
+        getattr(m, k)[: len(ref_map[k])].copy_(torch.from_numpy(ref_map[k]))
+    m.n_points, m.n_intervals = ref_map["n_points"], ref_map["n_intervals"]
+    out = gpu_forward(wl, m, depth, feat)
+    torch.cuda.synchronize()
+    assert_forward_close(wl, out, oracle_forward(wl))
+
+
+# ---------------------------------------------------------------- channel counts and dtypes
+
+SUPPORTED_C = [8, 16, 32, 64, 80, 96, 128, 160, 192, 256]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "e4m3"])
+@pytest.mark.parametrize("C", SUPPORTED_C)
+def test_every_channel_count(bp, C, dtype):
+    from depth_weighted_scatter_gb300 import workloads
+
+    NC, D, H, W, cells = 3, 17, 6, 11, 700
+    rng = np.random.default_rng(C * 7 + (dtype == "e4m3"))
+    nf = NC * D * H * W
+    cid = rng.integers(0, cells, nf).astype(np.int32)
+    cid[rng.random(nf) < 0.3] = -1
+    cid[rng.random(nf) < 0.08] = 123                 # one long interval (several owners share it)
+    wl = workloads.custom(NC, D, H, W, C, cells, cid, seed=C, dtype=dtype, name=f"C{C}_{dtype}")
+    c_d, depth, feat = upload(wl)
+    m = _gpu_map(bp, wl, c_d)
+    _check_map(bp, wl, m)
+    out = torch.full((cells, C), float("nan"), dtype=torch.float16, device="cuda")
+    gpu_forward(wl, m, depth, feat, out=out)
+    torch.cuda.synchronize()
+    assert_forward_close(wl, out, oracle_forward(wl))
+
+
+# ---------------------------------------------------------------- edge cases
+
+def _edge(bp, cid, NC, D, H, W, C, cells, name, dtype="f16", seed=0):
+    from depth_weighted_scatter_gb300 import workloads
+
+    wl = workloads.custom(NC, D, H, W, C, cells, np.asarray(cid, np.int32), seed=seed, dtype=dtype, name=name)
+    c_d, depth, feat = upload(wl)
+    m = _gpu_map(bp, wl, c_d)
+    _check_map(bp, wl, m)
+    out = torch.full((cells, C), float("nan"), dtype=torch.float16, device="cuda")
+    gpu_forward(wl, m, depth, feat, out=out)
+    torch.cuda.synchronize()
+    assert_forward_close(wl, out, oracle_forward(wl))
+    return m, out
+
+
+def test_edge_all_dropped(bp):
+    m, out = _edge(bp, np.full(2 * 3 * 4 * 5, -1), 2, 3, 4, 5, 64, 50, "all_dropped")
+    assert m.n_points == 0 and m.n_intervals == 0
+    assert torch.count_nonzero(out) == 0
+
+
+def test_edge_single_cell_grid(bp):
+    _edge(bp, np.zeros(1 * 6 * 5 * 7), 1, 6, 5, 7, 80, 1, "one_cell")
+
+
+def test_edge_one_interval_of_20000_points(bp):
+    NC, D, H, W = 2, 50, 10, 20                       # 20,000 frustum points, all in cell 5
+    _edge(bp, np.full(NC * D * H * W, 5), NC, D, H, W, 80, 9, "long_interval")
+
+
+def test_edge_every_cell_hit_once(bp):
+    NC, D, H, W = 2, 1, 16, 32
+    nf = NC * D * H * W
+    _edge(bp, np.random.default_rng(4).permutation(nf), NC, D, H, W, 64, nf, "bijection")
+
+
+def test_edge_ragged_tiles_and_many_cells(bp):
+    """Frustum not a multiple of the 4096-point tile; cell ids need 31 bits (3 radix passes)."""
+    NC, D, H, W = 1, 37, 13, 11                       # 5291 points: one full tile + a ragged one
+    rng = np.random.default_rng(11)
+    cells = (1 << 31) - 1
+    cid = rng.integers(0, 40, NC * D * H * W).astype(np.int64) * 50_000_000 + rng.integers(0, 3, NC * D * H * W)
+    cid[rng.random(cid.size) < 0.2] = -1
+    from depth_weighted_scatter_gb300 import workloads
+    import oracle
+
+    wl = workloads.custom(NC, D, H, W, 8, cells, cid.astype(np.int32), seed=11, name="wide_keys")
+    c_d, depth, feat = upload(wl)
+    m = _gpu_map(bp, wl, c_d)
+    _check_map(bp, wl, m)
+
+
+def test_edge_out_of_range_ids_flagged(bp):
+    NC, D, H, W, cells = 1, 4, 8, 8, 64
+    rng = np.random.default_rng(12)
+    cid = rng.integers(0, cells, NC * D * H * W).astype(np.int32)
+    cid[[3, 77, 200]] = [-5, cells, 1 << 30]
+    c_d = torch.from_numpy(cid).cuda()
+    with pytest.raises(bp.BevpoolError) as ei:
+        bp.build_map(c_d, NC, D, H, W, cells)
+    assert ei.value.status == bp.BEVPOOL_ERR_OUT_OF_RANGE
+    m = bp.build_map(c_d, NC, D, H, W, cells, sync=False)
+    counts = m.d_counts.cpu().numpy()
+    assert counts[2] == 3                             # three invalid ids, treated as dropped
+    import oracle
+
+    good = cid.copy()
+    good[[3, 77, 200]] = -1
+    ref = oracle.build_map(good, NC, D, H, W, cells)
+    got = m.host()
+    for k in MAP_KEYS:
+        assert np.array_equal(got[k], ref[k])
+
+
+def test_validate_map_flags_corruption(bp, wl_cache):
+    wl = wl_cache("tiny")
+    cells, _, _ = upload(wl)
+    m = _gpu_map(bp, wl, cells)
+    assert bp.validate_map(m) == 0
+    m.interval_lengths[0] += 1
+    assert bp.validate_map(m) & (1 | 2)
+    m.interval_lengths[0] -= 1
+    m.ranks_feat[0] = wl.n_feat_rows
+    assert bp.validate_map(m) & 32
+
+
+def test_forward_rejects_bad_arguments(bp, wl_cache):
+    wl = wl_cache("tiny")
+    cells, depth, feat = upload(wl)
+    m = _gpu_map(bp, wl, cells)
+    with pytest.raises(bp.BevpoolError) as ei:
+        bp.forward(m, depth, feat, 24)
+    assert ei.value.status == bp.BEVPOOL_ERR_UNSUPPORTED
+    out = torch.empty(wl.n_cells * wl.C + 8, dtype=torch.float16, device="cuda")
+    with pytest.raises(bp.BevpoolError) as ei:
+        bp.forward(m, depth, feat, wl.C, out=out[1:])     # misaligned output
+    assert ei.value.status == bp.BEVPOOL_ERR_INVALID_ARG
