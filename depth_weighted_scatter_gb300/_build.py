@@ -27,7 +27,8 @@ def nvcc() -> str:
 
 
 def common_flags() -> list:
-    return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+    extra = os.environ.get("BEVPOOL_NVCC_EXTRA", "").split()   # developer knob, e.g. -DBEVPOOL_FMA_VARIANT=0
+    return ARCH + extra + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
                    "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
 
 

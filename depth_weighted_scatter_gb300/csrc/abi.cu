@@ -241,6 +241,7 @@ bevpool_status bevpool_forward(bevpool_dtype dtype, const void *depth, const voi
                               nf * eb + static_cast<int64_t>(a.n_feat_rows) * C * eb +
                               static_cast<int64_t>(n_cells) * C * 2;
     a.streaming_stores = footprint > static_cast<int64_t>(info.l2_bytes) / 2 ? 1 : 0;
+    a.sm_count = info.sm_count;
     a.out = out;
     a.stream = static_cast<cudaStream_t>(stream);
     const cudaError_t e = dtype == BEVPOOL_F16 ? launch_forward_f16(a) : launch_forward_e4m3(a);

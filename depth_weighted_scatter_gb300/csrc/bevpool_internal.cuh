@@ -123,6 +123,7 @@ struct ForwardArgs {
     int32_t n_feat_rows;      // NC*H*W
     float scale;              // depth_scale * feat_scale
     int streaming_stores;     // 1: evict-first output stores (HBM regime)
+    int sm_count;             // SMs of the current device (launch sizing)
     void *out;
     cudaStream_t stream;
 };

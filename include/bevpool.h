@@ -130,7 +130,9 @@ BEVPOOL_API bevpool_status bevpool_build_map(const int32_t *cell_ids, int32_t NC
  * scale = depth_scale * feat_scale, accumulated in FP32 and rounded once to
  * fp16 (round to nearest even).  Every one of the n_cells rows of `out` is
  * written exactly once; rows no interval names are written as zeros.  No
- * atomics: the result is bit-identical from run to run.
+ * atomics: calls with identical arguments give bit-identical results (the
+ * work split, and so the FP32 summation order inside intervals longer than
+ * 32 points, depends on n_intervals and the device's SM count).
  *
  *   dtype             BEVPOOL_F16 or BEVPOOL_E4M3 (depth and feat alike).
  *   depth             device, [NC, D, H, W] elements of dtype.

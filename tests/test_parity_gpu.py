@@ -66,15 +66,21 @@ def test_forward_is_deterministic(bp, name, wl_cache):
 
 
 def test_device_counts_path_matches_host_counts(bp, wl_cache):
-    """build_map without a host sync, forward reading the counts on the device."""
+    """build_map without a host sync, forward reading the counts on the device.
+
+    With capacities equal to the counts the launch is the same, so the bits
+    are; with larger capacities the interval chunking (and with it the split
+    points of long intervals) may differ, so only the tolerance holds."""
     wl = wl_cache("canonical")
     cells, depth, feat = upload(wl)
     m_sync = _gpu_map(bp, wl, cells)
     m_async = _gpu_map(bp, wl, cells, sync=False)
     a = gpu_forward(wl, m_sync, depth, feat)
-    b = gpu_forward(wl, m_async, depth, feat, capacity=(m_sync.n_points + 1000, m_sync.n_intervals + 500))
+    b = gpu_forward(wl, m_async, depth, feat, capacity=(m_sync.n_points, m_sync.n_intervals))
+    c = gpu_forward(wl, m_async, depth, feat, capacity=(m_sync.n_points + 1000, m_sync.n_intervals + 5000))
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert_forward_close(wl, c, oracle_forward(wl))
 
 
 def test_forward_on_oracle_map(bp, wl_cache):
