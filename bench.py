@@ -174,6 +174,13 @@ def max_over_ranks(values, world: int, device):
     return t.tolist()
 
 
+def config_dict(wl, n_pts: int, n_int: int, world: int) -> dict:
+    return {"workload": f"{wl.name}: NC={wl.NC} D={wl.D} H={wl.H} W={wl.W} C={wl.C} grid={wl.grid} "
+                        f"points={n_pts} intervals={n_int}",
+            "l2": "flushed (256 MiB written) before the map build and before the forward",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def cpu_oracle_time(wl, budget_s: float = 10.0, max_reps: int = 50) -> dict:
     """Times the oracle's forward on the full workload, single-threaded."""
     import oracle
@@ -202,6 +209,7 @@ def run_reference(args) -> None:
 
     wl = workloads.make(args.config)
     oracle.build()
+    m = oracle.build_map(wl.cell_ids, *wl.dims(), wl.n_cells)
     call = lambda: oracle.forward(wl.dtype, wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat,
                                   wl.depth_scale, wl.feat_scale)
     for _ in range(args.warmup):
@@ -215,7 +223,7 @@ def run_reference(args) -> None:
     line = {"metric": METRIC, "value": v, "unit": "us/call", "impl": "reference", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "points": wl.n_kept, "C": wl.C, "n_cells": wl.n_cells},
+            "config": config_dict(wl, m["n_points"], m["n_intervals"], world),
             "cpu_baseline": {"value": v, "unit": "us/call", "cores": 1, "kind": "oracle",
                              "sample": f"each step one full {wl.name} forward of the single-threaded FP64 C oracle"},
             "e2e": {"value": v, "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -368,10 +376,7 @@ def run_ours(args) -> None:
         "vs_baseline": None,
         "dtype": wl.dtype,
         "data": "synthetic (seeded generator shaped like the pages' workload; nuScenes not used)",
-        "config": {"workload": f"{wl.name}: NC={wl.NC} D={wl.D} H={wl.H} W={wl.W} C={wl.C} grid={wl.grid} "
-                               f"points={n_pts} intervals={n_int}",
-                   "l2": "flushed (256 MiB written) before the map build and before the forward",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": config_dict(wl, n_pts, n_int, world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(wl.name),
                      "kernel": "k_forward", "bytes_per_launch": bm["footprint"],
