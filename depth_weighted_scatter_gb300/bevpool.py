@@ -37,6 +37,7 @@ BEVPOOL_ERR_WORKSPACE = 4
 BEVPOOL_ERR_CUDA = 5
 BEVPOOL_F16 = 0
 BEVPOOL_E4M3 = 1
+BEVPOOL_NOALLOC_MAX_FRUSTUM = 1 << 21
 
 _i32, _i64, _sz, _vp, _f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
 
@@ -52,6 +53,8 @@ _lib.bevpool_build_map_workspace_size.argtypes = [_i64, _i32]
 _lib.bevpool_build_map_workspace_size.restype = _sz
 _lib.bevpool_build_map.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
 _lib.bevpool_build_map.restype = ctypes.c_int
+_lib.bevpool_build_map_noalloc.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+_lib.bevpool_build_map_noalloc.restype = ctypes.c_int
 _lib.bevpool_forward.argtypes = [ctypes.c_int, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _f32,
                                  _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp]
 _lib.bevpool_forward.restype = ctypes.c_int
@@ -98,6 +101,14 @@ def bevpool_build_map(cell_ids: int, NC: int, D: int, H: int, W: int, n_cells: i
     return _lib.bevpool_build_map(cell_ids, NC, D, H, W, n_cells, ranks_depth, ranks_feat, ranks_bev,
                                   interval_starts, interval_lengths, d_counts, _host_ptr(h_counts), workspace,
                                   workspace_bytes, stream)
+
+
+def bevpool_build_map_noalloc(cell_ids: int, NC: int, D: int, H: int, W: int, n_cells: int, ranks_depth: int,
+                              ranks_feat: int, ranks_bev: int, interval_starts: int, interval_lengths: int,
+                              d_counts: int, h_counts: Optional[np.ndarray], stream: int) -> int:
+    """bevpool_build_map with the library's built-in scratch (no workspace, no allocation)."""
+    return _lib.bevpool_build_map_noalloc(cell_ids, NC, D, H, W, n_cells, ranks_depth, ranks_feat, ranks_bev,
+                                          interval_starts, interval_lengths, d_counts, _host_ptr(h_counts), stream)
 
 
 def bevpool_forward(dtype: int, depth: int, feat: int, NC: int, D: int, H: int, W: int, C: int,

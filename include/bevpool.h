@@ -122,6 +122,35 @@ BEVPOOL_API bevpool_status bevpool_build_map(const int32_t *cell_ids, int32_t NC
                                  size_t workspace_bytes, void *stream);
 
 /*
+ * bevpool_build_map without a workspace argument, for callers that may not
+ * allocate device memory (for example an inference-engine plugin whose
+ * enqueue step must not allocate, or real-time code that forbids allocation
+ * after start-up).  The pages have no counterpart to this entry point: it is
+ * an interface convenience of this library.
+ *
+ * It runs the same kernels and gives the same results as bevpool_build_map,
+ * with the same arguments and outputs, but its scratch is a fixed array of
+ * BEVPOOL_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU
+ * that loads the library holds until the process exits.  It calls no
+ * allocating routine.
+ *   - NC*D*H*W must not exceed BEVPOOL_NOALLOC_MAX_FRUSTUM; larger frusta
+ *     return BEVPOOL_ERR_WORKSPACE and enqueue nothing.
+ *   - All calls on a device share the array: calls whose work may overlap on
+ *     the GPU (other streams, other host threads) race and must be ordered by
+ *     the caller.  Nothing in the array needs clearing between calls.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress), which cannot happen during stream capture: make
+ *     the first call on a device outside any capture.
+ */
+#define BEVPOOL_NOALLOC_MAX_FRUSTUM (1 << 21)
+#define BEVPOOL_NOALLOC_SCRATCH_BYTES (37u * 1024u * 1024u)
+BEVPOOL_API bevpool_status bevpool_build_map_noalloc(const int32_t *cell_ids, int32_t NC, int32_t D, int32_t H,
+                                         int32_t W, int32_t n_cells, int32_t *ranks_depth,
+                                         int32_t *ranks_feat, int32_t *ranks_bev,
+                                         int32_t *interval_starts, int32_t *interval_lengths,
+                                         int32_t *d_counts, int32_t *h_counts, void *stream);
+
+/*
  * Interval-owned forward (sections "Eliminate redundant scatter traffic"
  * and "Implement interval-owned scatter-reduce"): for every interval i,
  *     out[ranks_bev[s], c] = scale * sum_{t in [s, s+len)}
