@@ -37,7 +37,7 @@ def _sources() -> list:
 
 
 def _deps() -> list:
-    return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [
+    return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))) + [
         os.path.join(ROOT, "include", "bevpool.h"), os.path.abspath(__file__)]
 
 

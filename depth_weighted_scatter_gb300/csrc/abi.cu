@@ -164,8 +164,11 @@ bevpool_status bevpool_build_map(const int32_t *cell_ids, int32_t NC, int32_t D,
     for (const void *p : ptrs)
         if (!aligned(p, 4)) return BEVPOOL_ERR_INVALID_ARG;
     const int64_t nf = static_cast<int64_t>(NC) * D * H * W;
-    if (!workspace || !aligned(workspace, 256) || workspace_bytes < build_map_workspace_bytes(nf, n_cells))
-        return BEVPOOL_ERR_WORKSPACE;
+    if (!workspace || !aligned(workspace, 256)) return BEVPOOL_ERR_WORKSPACE;
+    // Counting-sort path when the grid is small enough and the workspace holds
+    // it; otherwise the radix path (smaller for huge grids).
+    const bool counting = n_cells <= kCountingMaxCells && workspace_bytes >= count_workspace_bytes(nf, n_cells);
+    if (!counting && workspace_bytes < radix_workspace_bytes(nf)) return BEVPOOL_ERR_WORKSPACE;
 
     BuildMapArgs a;
     a.cell_ids = cell_ids;
@@ -182,6 +185,7 @@ bevpool_status bevpool_build_map(const int32_t *cell_ids, int32_t NC, int32_t D,
     a.d_counts = d_counts;
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
+    a.counting = counting;
     a.stream = static_cast<cudaStream_t>(stream);
     bevpool_status st = cuda_status(launch_build_map(a));
     if (st != BEVPOOL_OK || !h_counts) return st;

@@ -8,6 +8,7 @@
 #include <atomic>
 
 #include "../../include/bevpool.h"
+#include "fastdiv.h"
 
 namespace bevpool {
 
@@ -107,10 +108,17 @@ struct BuildMapArgs {
     int32_t *d_counts;
     void *workspace;
     size_t workspace_bytes;
+    bool counting;            // counting-sort path (n_cells <= kCountingMaxCells) or radix path
     cudaStream_t stream;
 };
-size_t build_map_workspace_bytes(int64_t n_frustum, int32_t n_cells);
+// Grids up to this many cells use the counting-sort map build; larger ones the radix sort.
+constexpr int32_t kCountingMaxCells = 1 << 24;
+size_t build_map_workspace_bytes(int64_t n_frustum, int32_t n_cells);   // preferred path
+size_t radix_workspace_bytes(int64_t n_frustum);
+size_t count_workspace_bytes(int64_t n_frustum, int32_t n_cells);
 cudaError_t launch_build_map(const BuildMapArgs &a);
+cudaError_t launch_build_map_radix(const BuildMapArgs &a);
+cudaError_t launch_build_map_counting(const BuildMapArgs &a);
 
 // Forward (forward_f16.cu / forward_e4m3.cu).
 struct ForwardArgs {

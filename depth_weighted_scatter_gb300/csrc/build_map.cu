@@ -1,4 +1,6 @@
-// build_map.cu -- scatter-map construction on the GPU (sm_103a).
+// build_map.cu -- scatter-map construction on the GPU (sm_103a): the radix
+// path, used for grids of more than kCountingMaxCells cells (build_map_count.cu
+// handles the rest), and the dispatch between the two.
 //
 // Builds the five-array INT32 scatter map of "Accelerating BEV Pooling on
 // NVIDIA GPUs for Physical AI Applications" (section "Eliminate redundant
@@ -434,11 +436,17 @@ k_emit(const int32_t *__restrict__ bev, const int32_t *__restrict__ n_dev,
 
 }  // namespace
 
-size_t build_map_workspace_bytes(int64_t n_frustum, int32_t /*n_cells*/) {
-    return carve(nullptr, n_frustum, nullptr);
+size_t radix_workspace_bytes(int64_t n_frustum) { return carve(nullptr, n_frustum, nullptr); }
+
+size_t build_map_workspace_bytes(int64_t n_frustum, int32_t n_cells) {
+    return n_cells <= kCountingMaxCells ? count_workspace_bytes(n_frustum, n_cells) : radix_workspace_bytes(n_frustum);
 }
 
 cudaError_t launch_build_map(const BuildMapArgs &a) {
+    return a.counting ? launch_build_map_counting(a) : launch_build_map_radix(a);
+}
+
+cudaError_t launch_build_map_radix(const BuildMapArgs &a) {
     const int64_t nf = static_cast<int64_t>(a.NC) * a.D * a.H * a.W;
     const int nt = static_cast<int>(div_up(nf, kTile));
     Workspace ws;

@@ -71,8 +71,10 @@ extern "C" bevpool_status bevpool_build_map_noalloc(const int32_t *cell_ids, int
     if (NC < 1 || D < 1 || H < 1 || W < 1 || n_cells < 1) return BEVPOOL_ERR_INVALID_ARG;
     const int64_t nf = static_cast<int64_t>(NC) * D * H * W;
     if (nf > BEVPOOL_NOALLOC_MAX_FRUSTUM) return BEVPOOL_ERR_WORKSPACE;   // larger than the built-in scratch
-    const size_t need = build_map_workspace_bytes(nf, n_cells);
-    if (need > kNoallocScratchBytes) return BEVPOOL_ERR_WORKSPACE;
+    // bevpool_build_map takes the counting-sort path when its workspace fits in
+    // the scratch and the radix path otherwise; the radix path always fits for
+    // frusta up to the limit.
+    if (radix_workspace_bytes(nf) > kNoallocScratchBytes) return BEVPOOL_ERR_WORKSPACE;
     void *scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess) {
         cudaGetLastError();

@@ -76,7 +76,10 @@ def test_workspace_size(bp):
     small = bp.bevpool_build_map_workspace_size(4096, 100)
     big = bp.bevpool_build_map_workspace_size(1_993_728, 129_600)
     assert 0 < small < big
-    assert big >= 4 * 4 * 1_993_728       # two key/value buffers of int32
+    # counting-sort path: grouped frustum indices + two per-cell tables
+    assert big >= 4 * 1_993_728 + 2 * 4 * 129_600
+    # grids above 2^24 cells take the radix path: two key/value buffers of int32
+    assert bp.bevpool_build_map_workspace_size(1_993_728, (1 << 24) + 1) >= 4 * 4 * 1_993_728
 
 
 FAKE = 1 << 20   # never dereferenced: every call below fails validation first

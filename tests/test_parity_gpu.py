@@ -178,6 +178,21 @@ def test_edge_ragged_tiles_and_many_cells(bp):
     _check_map(bp, wl, m)
 
 
+def test_edge_radix_path_just_above_counting_limit(bp):
+    """A grid one cell bigger than the counting-sort limit takes the radix path (25-bit keys)."""
+    from depth_weighted_scatter_gb300 import workloads
+
+    NC, D, H, W = 2, 9, 17, 19
+    nf = NC * D * H * W
+    cells = (1 << 24) + 1
+    rng = np.random.default_rng(21)
+    cid = np.where(rng.random(nf) < 0.5, rng.integers(0, 300, nf), rng.integers(cells - 300, cells, nf))
+    cid[rng.random(nf) < 0.1] = -1
+    wl = workloads.custom(NC, D, H, W, 8, cells, cid.astype(np.int32), seed=21, name="radix_path")
+    c_d, _, _ = upload(wl)
+    _check_map(bp, wl, _gpu_map(bp, wl, c_d))
+
+
 def test_edge_out_of_range_ids_flagged(bp):
     NC, D, H, W, cells = 1, 4, 8, 8, 64
     rng = np.random.default_rng(12)
