@@ -21,7 +21,7 @@
 //                    points in registers (a bitonic network); longer
 //                    intervals go to two work lists;
 //   7. k_sort_lists  persistent CTAs drain the lists: a warp ranks an interval
-//                    of up to 256 points by counting (rank = number of smaller
+//                    of up to 64 points by counting (rank = number of smaller
 //                    values), a CTA sorts up to 8192 in shared memory
 //                    (bitonic), and beyond that the CTA rebuilds the run by
 //                    scanning the frustum in order for that cell.
@@ -41,7 +41,7 @@ constexpr int kTile = kThreads * kItems;        // 4096 frustum points per CTA t
 constexpr int kCellItems = 4;
 constexpr int kCellTile = kThreads * kCellItems; // 1024 cells per scan tile
 constexpr int kThreadSortMax = 16;              // longest interval one thread sorts in registers
-constexpr int kWarpSortMax = 256;               // longest interval a warp ranks
+constexpr int kWarpSortMax = 64;                // longest interval a warp ranks
 constexpr int kCtaSortMax = 8192;               // longest interval sorted in shared memory
 
 struct CountWs {
@@ -53,8 +53,8 @@ struct CountWs {
     int32_t *tile_nz;     // [cell tiles]
     int32_t *invalid;     // [1]
     int32_t *lists;       // [2]: entries in mid_list, long_list
-    int32_t *mid_list;    // [min(n_frustum, n_cells)] intervals of 17..256 points
-    int32_t *long_list;   // [min(n_frustum, n_cells)] intervals of more than 256 points
+    int32_t *mid_list;    // [min(n_frustum, n_cells)] intervals of 17..64 points
+    int32_t *long_list;   // [min(n_frustum, n_cells)] intervals of more than 64 points
 };
 
 size_t carve(void *base, int64_t nf, int32_t n_cells, CountWs *ws) {
@@ -227,38 +227,37 @@ struct Derive {
     }
 };
 
-// One warp ranks an interval of L <= 256 points: each lane holds up to 8
-// values; a value's rank is the number of smaller values (p are distinct).
+// One warp ranks an interval of L <= 32*R points: each lane holds R values; a
+// value's rank is the number of smaller values (p are distinct).
+template <int R>
 __device__ __forceinline__ void warp_rank_sort(const int32_t *__restrict__ src, int s, int L, int cell,
                                                const Derive &out) {
     const int lane = threadIdx.x & 31;
-    constexpr int R = kWarpSortMax / 32;
-    const int nv = (L + 31) >> 5;
     int v[R], rank[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int idx = r * 32 + lane;
-        v[r] = (r < nv && idx < L) ? __ldg(src + s + idx) : INT_MAX;
+        v[r] = idx < L ? __ldg(src + s + idx) : INT_MAX;
         rank[r] = 0;
     }
 #pragma unroll
     for (int r2 = 0; r2 < R; ++r2) {
-        if (r2 >= nv) break;                                   // uniform over the warp
-        const int kmax = min(32, L - r2 * 32);
+        const int kmax = min(32, L - r2 * 32);                 // uniform over the warp
+#pragma unroll 4
         for (int k = 0; k < kmax; ++k) {
             const int x = __shfl_sync(0xffffffffu, v[r2], k);
 #pragma unroll
-            for (int r = 0; r < R; ++r) rank[r] += (r < nv) & (x < v[r]);
+            for (int r = 0; r < R; ++r) rank[r] += x < v[r];
         }
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int idx = r * 32 + lane;
-        if (r < nv && idx < L) out.put(s + rank[r], v[r], cell);
+        if (idx < L) out.put(s + rank[r], v[r], cell);
     }
 }
 
-// The CTA sorts an interval of 256 < L <= 8192 points in shared memory.
+// The CTA sorts an interval of 64 < L <= 8192 points in shared memory.
 __device__ __forceinline__ void cta_bitonic_sort(const int32_t *__restrict__ src, int s, int L, int cell,
                                                  const Derive &out, int *buf) {
     int n2 = 1;
@@ -371,7 +370,11 @@ k_sort_lists(const int32_t *__restrict__ tmp_p, const int32_t *__restrict__ star
     const int warps_total = gridDim.x * kWarps;
     for (int x = blockIdx.x * kWarps + (threadIdx.x >> 5); x < n_mid; x += warps_total) {   // warp-uniform
         const int j = __ldg(mid_list + x);
-        warp_rank_sort(tmp_p, __ldg(starts + j), __ldg(lengths + j), __ldg(icell + j), out);
+        const int L = __ldg(lengths + j);
+        if (L <= 32)
+            warp_rank_sort<1>(tmp_p, __ldg(starts + j), L, __ldg(icell + j), out);
+        else
+            warp_rank_sort<2>(tmp_p, __ldg(starts + j), L, __ldg(icell + j), out);
     }
     for (int x = blockIdx.x; x < n_long; x += gridDim.x) {                                // CTA-uniform
         const int j = __ldg(long_list + x);
@@ -418,7 +421,7 @@ cudaError_t launch_build_map_counting(const BuildMapArgs &a) {
         ws.tmp_p, a.interval_starts, a.interval_lengths, ws.icell, a.d_counts, ws.lists, ws.mid_list, ws.long_list,
         out);
     count_launch();
-    k_sort_lists<<<info.sm_count * 2, kThreads, 0, st>>>(ws.tmp_p, a.interval_starts, a.interval_lengths, ws.icell,
+    k_sort_lists<<<info.sm_count * 4, kThreads, 0, st>>>(ws.tmp_p, a.interval_starts, a.interval_lengths, ws.icell,
                                                         ws.lists, ws.mid_list, ws.long_list, a.cell_ids, nf, out);
     count_launch();
     return cudaGetLastError();
