@@ -11,21 +11,20 @@
 // One launch, two kinds of CTA (interleaved in blockIdx so both run from the
 // first wave):
 //
-//   compute CTA  owns a chunk of consecutive intervals.  An owner is the LPO
-//                lanes that together hold one C-channel row (VB bytes per
-//                lane).  Each interval is cut into pieces of at most kPiece
-//                points; owners take pieces round-robin.  A one-piece interval
-//                (the common case: the canonical workload averages 3.6 points)
-//                is reduced and written by its owner alone.  Pieces of a longer
-//                interval leave FP32 partial rows in shared memory; after a
-//                barrier the owner of the interval's first piece in the round
-//                adds them in piece order (plus a carry from the previous
-//                round), so the sum order is fixed and the result
-//                deterministic.  Per point: one depth load ("depth loaded once
-//                per scatter point"), one feature-row gather, FP32 FMAs; up to
-//                four points are in flight per owner.  Point indices are
-//                fetched cooperatively (each lane loads a different point's
-//                ranks, warp shuffles broadcast them).
+//   compute CTA  owns a chunk of consecutive intervals, i.e. a contiguous
+//                range of the sorted point arrays.  An owner is the LPO lanes
+//                that together hold one C-channel row (VB bytes per lane).
+//                Owners take equal shares of the chunk's points and walk them
+//                in lockstep, BATCH points at a time: each lane fetches one
+//                point's ranks, warp shuffles broadcast them, and each owner
+//                then has BATCH depth loads and feature-row gathers in flight
+//                ("depth loaded once per scatter point").  An interval ends
+//                where ranks_bev changes, so the ends of a batch are one
+//                bit mask, known before its FMAs; at an end the owner rounds
+//                its FP32 row to fp16 and stores it.  An interval cut by a
+//                share boundary leaves FP32 partial rows in shared memory;
+//                after a barrier the owner that started it adds them in owner
+//                order, so the sum order is fixed and the result deterministic.
 //
 //   fill CTA     owns a tile of kFillCells consecutive cells.  It finds the
 //                tile's points in the sorted ranks_bev with a CTA-wide k-ary
@@ -34,6 +33,8 @@
 //                This keeps the (large, uneven) empty regions of the grid off
 //                the interval owners and spreads them evenly over the GPU.
 #pragma once
+
+#include <climits>
 
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -60,7 +61,15 @@ namespace bevpool {
 constexpr int kDtypeF16 = 0;
 constexpr int kDtypeE4M3 = 1;
 constexpr int kFillCells = 256;
-constexpr int kMaxChunk = 1024;     // max intervals per compute CTA
+// Compute CTAs per SM (one wave of them): with the output resident in L2,
+// two, leaving a slot for fill CTAs to run alongside; when the output streams
+// to DRAM, three (the gathers need the issue slots more than the fills).
+#ifndef BEVPOOL_FWD_CTAS_PER_SM_L2
+#define BEVPOOL_FWD_CTAS_PER_SM_L2 2
+#endif
+#ifndef BEVPOOL_FWD_CTAS_PER_SM_DRAM
+#define BEVPOOL_FWD_CTAS_PER_SM_DRAM 3
+#endif
 
 template <int DT, int C>
 struct FwdShape {
@@ -98,7 +107,7 @@ struct FwdParams {
     float scale;
     int streaming;
     int n_compute;                // compute CTAs
-    int ipc;                      // intervals per compute CTA (<= kMaxChunk)
+    FastDiv n_compute_div;        // division by n_compute
     int n_fill;                   // fill CTAs
     __half *out;
 };
@@ -239,11 +248,14 @@ __device__ __forceinline__ void store_row_part(__half *dst, const float *acc, fl
 template <int DT, int C>
 struct ComputeSmem {
     using S = FwdShape<DT, C>;
-    int pre[kMaxChunk + 1];                       // exclusive prefix of interval lengths
-    int bev[kMaxChunk];                           // output row of each interval (-1: skip)
-    int len[kMaxChunk];
-    __align__(16) float slot[2][S::OWNERS][C];    // partial rows of split (long) intervals
+    int state[S::OWNERS];                         // how an owner's share starts (kHead / kCont / kPass)
+    __align__(16) float slot[2][S::OWNERS][C];    // partial rows of intervals cut by a share boundary
 };
+
+// How an owner's share of the chunk starts:
+constexpr int kHead = 0;   // at the first point of an interval (or the share is empty)
+constexpr int kCont = 1;   // inside an interval that ends within the share: its partial is in slot[0]
+constexpr int kPass = 2;   // inside an interval that runs through the whole share: its partial is in slot[0]
 
 struct FillSmem {
     unsigned mark[kFillCells / 32];
@@ -254,203 +266,6 @@ union FwdSmem {
     ComputeSmem<DT, C> c;
     FillSmem f;
 };
-
-// Interval k of the chunk that holds virtual point v (pre[k] <= v < pre[k+1]),
-// for 0 <= v < pre[nI]; empty intervals are never returned.
-__device__ __forceinline__ int interval_of(const int *pre, int nI, int v) {
-    int lo = 0, hi = nI;                           // pre[lo] <= v < pre[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (pre[mid] <= v) lo = mid; else hi = mid;
-    }
-    return lo;
-}
-
-// Writes acc (one owner's share of a row) either to the output row or to a
-// partial slot in shared memory.
-template <int DT, int C>
-__device__ __forceinline__ void flush_row(const FwdParams &p, ComputeSmem<DT, C> &sm, const float *acc, int bev,
-                                          int where, int o, int ol) {
-    using S = FwdShape<DT, C>;
-    if (where < 0) {
-        if (bev >= 0)
-            store_row_part<S::EPL>(p.out + static_cast<int64_t>(bev) * C + ol * S::EPL, acc, p.scale, p.streaming);
-    } else {
-        float *dst = &sm.slot[where][o][ol * S::EPL];
-#pragma unroll
-        for (int e = 0; e < S::EPL; ++e) dst[e] = acc[e];
-    }
-}
-
-template <int DT, int C>
-__device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, ComputeSmem<DT, C> &sm) {
-    using S = FwdShape<DT, C>;
-    __shared__ int scratch[kWarps + 1];
-    __shared__ int s_t0;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-
-    int n_int = p.n_intervals, n_pts = p.n_points;
-    if (p.d_counts) {
-        n_int = min(n_int, __ldg(p.d_counts + 1));
-        n_pts = min(n_pts, __ldg(p.d_counts + 0));
-    }
-    const int ipc = p.ipc;
-    const int i0 = cidx * ipc;
-    if (i0 >= n_int) return;                       // uniform over the CTA
-    const int nI = min(ipc, n_int - i0);
-
-    // 1. chunk metadata: thread t owns intervals [t*ipt, t*ipt + ipt) (blocked, for the scan)
-    const int ipt = (ipc + kThreads - 1) / kThreads;
-    const int kb = threadIdx.x * ipt;
-    int my_sum = 0;
-    bool ok = true;
-    int prev_end = -1;
-    int first_start = -1;
-    for (int q = 0; q < ipt; ++q) {
-        const int k = kb + q;
-        if (k >= nI) break;
-        const int s = __ldg(p.starts + i0 + k);
-        int L = __ldg(p.lengths + i0 + k);
-        int cell = -1;
-        if (s < 0 || L < 1 || s > n_pts - L) {
-            ok = false;
-            L = 0;
-        } else {
-            cell = __ldg(p.ranks_bev + s);
-            if (cell < 0 || cell >= p.n_cells) cell = -1;
-        }
-        if (q == 0) first_start = s; else if (s != prev_end) ok = false;
-        prev_end = s + L;
-        sm.len[k] = L;
-        sm.bev[k] = cell;
-        my_sum += L;
-    }
-    if (threadIdx.x == 0) s_t0 = first_start;
-    int P;
-    const int excl = cta_exclusive_sum(my_sum, scratch, &P);   // has barriers: s_t0 visible after
-    for (int q = 0; q < ipt; ++q) {
-        const int k = kb + q;
-        if (k >= nI) break;
-        sm.pre[k] = excl + (q ? sm.pre[k - 1] - excl + sm.len[k - 1] : 0);
-    }
-    if (threadIdx.x == 0) sm.pre[nI] = P;
-    // contiguity across threads: my first interval must start where the chunk's
-    // points up to it end (start = t0 + prefix)
-    if (kb < nI && first_start != s_t0 + excl) ok = false;
-    const bool chunk_ok = __syncthreads_and(ok) != 0;
-    if (!chunk_ok) return;                          // malformed map: unspecified output, no OOB access
-    const int T0 = s_t0;
-
-    // 2. owners take equal shares of the chunk's points and walk them in
-    //    lockstep (same trip count for every owner of a warp); an interval cut
-    //    by a share boundary leaves partial rows for the combine below.
-    const int og = lane / S::LPO;                  // owner within warp
-    const int ol = lane % S::LPO;                  // lane within owner
-    const bool active = og < S::OPW;
-    const int o = active ? warp * S::OPW + og : 0;
-    const int lane0 = og * S::LPO;
-    const unsigned gmask = (S::LPO == 32 ? 0xffffffffu : ((1u << S::LPO) - 1u)) << lane0;
-    const unsigned char *featp = static_cast<const unsigned char *>(p.feat) + ol * S::VB;
-    const int share = (P + S::OWNERS - 1) / S::OWNERS;
-    const int beg = active ? min(P, o * share) : P;
-    const int end = active ? min(P, beg + share) : P;
-
-    int head_k = -1;
-    if (active) {
-        int k = beg < P ? interval_of(sm.pre, nI, beg) : nI - 1;
-        int next_end = sm.pre[k + 1];
-        bool seg_head = sm.pre[k] == beg;
-        float acc[S::EPL];
-#pragma unroll
-        for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
-        // indices of the first batch: lane ol holds point beg + ol (ol < BATCH)
-        int rd = -1, rf = -1;
-        auto fetch_idx = [&](int v0, int &ra, int &rb) {
-            ra = -1;
-            rb = -1;
-            const int j = v0 + ol;
-            if (ol < S::BATCH && j < end) {
-                const int x = __ldg(p.ranks_depth + T0 + j);
-                const int y = __ldg(p.ranks_feat + T0 + j);
-                if (x >= 0 && x < p.n_depth && y >= 0 && y < p.n_feat_rows) {
-                    ra = x;
-                    rb = y;
-                }
-            }
-        };
-        fetch_idx(beg, rd, rf);
-        for (int v0 = beg; v0 < beg + share; v0 += S::BATCH) {
-            int rd_next, rf_next;
-            fetch_idx(v0 + S::BATCH, rd_next, rf_next);      // prefetch the next batch's indices
-            int a[S::BATCH], b[S::BATCH];
-#pragma unroll
-            for (int kk = 0; kk < S::BATCH; ++kk) {
-                a[kk] = __shfl_sync(gmask, rd, lane0 + kk);
-                b[kk] = __shfl_sync(gmask, rf, lane0 + kk);
-            }
-            unsigned short d[S::BATCH];
-            RawVec<S::VB> f[S::BATCH];
-#pragma unroll
-            for (int kk = 0; kk < S::BATCH; ++kk) {
-                if (a[kk] >= 0) {
-                    d[kk] = load_depth_h<DT>(p.depth, a[kk]);
-                    f[kk] = load_vec<S::VB>(featp + static_cast<int64_t>(b[kk]) * S::ROWB);
-                } else {
-                    d[kk] = 0;
-#pragma unroll
-                    for (int i = 0; i < RawVec<S::VB>::NW; ++i) f[kk].w[i] = 0u;
-                }
-            }
-#pragma unroll
-            for (int kk = 0; kk < S::BATCH; ++kk) {
-                const int v = v0 + kk + 1;                   // points done after this one
-                if (v <= end) {
-                    fma_vec<DT, S::VB>(acc, d[kk], f[kk]);
-                    if (v == next_end) {                    // interval k ends with this point
-                        flush_row<DT, C>(p, sm, acc, sm.bev[k], seg_head ? -1 : 0, o, ol);
-#pragma unroll
-                        for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
-                        seg_head = true;
-                        if (v < end) {
-                            ++k;
-                            next_end = sm.pre[k + 1];
-                        }
-                    }
-                }
-            }
-            rd = rd_next;
-            rf = rf_next;
-        }
-        if (beg < end && end < next_end && end > sm.pre[k]) {   // share ends inside interval k
-            if (seg_head) {
-                flush_row<DT, C>(p, sm, acc, -1, 1, o, ol);
-                head_k = k;
-            } else {
-                flush_row<DT, C>(p, sm, acc, -1, 0, o, ol);
-            }
-        }
-    }
-
-    // 3. combine cut intervals in owner order
-    __syncthreads();
-    if (head_k >= 0) {
-        float acc[S::EPL];
-        const float *src = &sm.slot[1][o][ol * S::EPL];
-#pragma unroll
-        for (int e = 0; e < S::EPL; ++e) acc[e] = src[e];
-        const int stop = sm.pre[head_k + 1];
-        for (int o2 = o + 1; o2 < S::OWNERS; ++o2) {
-            const int b2 = min(P, o2 * share);
-            if (b2 >= stop) break;
-            const float *q = &sm.slot[0][o2][ol * S::EPL];
-#pragma unroll
-            for (int e = 0; e < S::EPL; ++e) acc[e] += q[e];
-        }
-        flush_row<DT, C>(p, sm, acc, sm.bev[head_k], -1, o, ol);
-    }
-}
-
-// ---------------------------------------------------------------- fill CTA
 
 // First index in [0, n) whose value is >= key, for two keys at once, by a
 // CTA-wide k-ary search over the sorted ranks_bev.
@@ -477,6 +292,201 @@ __device__ __forceinline__ void cta_lower_bound2(const int32_t *a, int n, int ke
     *r0 = lo0 + c0;
     *r1 = lo1 + c1;
 }
+
+// First interval start at or after x: the smallest t >= x with t == n or
+// ranks_bev[t] != ranks_bev[t - 1] (t == 0 counts as a start), for x0 and x1
+// at once.  One CTA-wide probe of kThreads points each; a window without a
+// start (an interval longer than kThreads) falls back to a k-ary search of
+// interval_starts.  Contains barriers.
+__device__ __forceinline__ void cta_next_starts(const FwdParams &p, int n, int n_int, int x0, int x1, int *t0,
+                                                int *t1, int *s) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x < 2) s[threadIdx.x] = INT_MAX;
+    __syncthreads();
+    const int i = threadIdx.x;
+    const int xs[2] = {x0, x1};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int x = xs[k];
+        bool hit = false;
+        if (i <= n - x) {                                   // t = x + i <= n
+            const int t = x + i;
+            hit = t == 0 || t == n || __ldg(p.ranks_bev + t) != __ldg(p.ranks_bev + t - 1);
+        }
+        const unsigned bal = __ballot_sync(0xffffffffu, hit);
+        if (lane == 0 && bal) atomicMin(&s[k], x + warp * 32 + __ffs(bal) - 1);
+    }
+    __syncthreads();
+    int r0 = s[0], r1 = s[1];
+    if (r0 == INT_MAX || r1 == INT_MAX) {                   // uniform over the CTA
+        int j0, j1;
+        cta_lower_bound2(p.starts, max(n_int, 0), x0, x1, &j0, &j1);
+        if (r0 == INT_MAX) r0 = j0 < n_int ? __ldg(p.starts + j0) : n;
+        if (r1 == INT_MAX) r1 = j1 < n_int ? __ldg(p.starts + j1) : n;
+    }
+    *t0 = min(max(r0, 0), n);
+    *t1 = min(max(r1, *t0), n);
+}
+
+template <int DT, int C>
+__device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, ComputeSmem<DT, C> &sm) {
+    using S = FwdShape<DT, C>;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+    __shared__ int s_bounds[2];
+    int n_int = p.n_intervals, n_pts = p.n_points;
+    if (p.d_counts) {
+        n_int = min(n_int, __ldg(p.d_counts + 1));
+        n_pts = min(n_pts, __ldg(p.d_counts + 0));
+    }
+    if (n_pts <= 0) return;                        // uniform over the CTA
+
+    // 1. the CTA's points: [cidx * ppc, (cidx + 1) * ppc) with both ends moved
+    //    forward to interval starts, so no interval is split between CTAs and
+    //    every CTA gets about the same number of points.
+    const int ppc = static_cast<int>(p.n_compute_div.div(static_cast<uint32_t>(n_pts - 1))) + 1;
+    const int64_t x0 = static_cast<int64_t>(cidx) * ppc;
+    if (x0 >= n_pts) return;
+    const int x1 = static_cast<int>(min(static_cast<int64_t>(n_pts), x0 + ppc));
+    int T0, T1;
+    cta_next_starts(p, n_pts, n_int, static_cast<int>(x0), x1, &T0, &T1, s_bounds);
+    if (T1 <= T0) return;                          // inside one long interval: the CTA before owns it
+    const int P = T1 - T0;
+
+    // 2. owners take equal shares of the chunk's points and walk them in
+    //    lockstep (same trip count for every owner of a warp).  A share that
+    //    starts inside an interval leaves its first partial row in slot[0]; a
+    //    share that ends inside an interval it started leaves a partial in
+    //    slot[1] and adds the later owners' slot[0] rows after the barrier.
+    const int og = lane / S::LPO;                  // owner within warp
+    const int ol = lane % S::LPO;                  // lane within owner
+    const bool active = og < S::OPW;
+    const int o = active ? warp * S::OPW + og : 0;
+    const int lane0 = og * S::LPO;
+    const unsigned gmask = (S::LPO == 32 ? 0xffffffffu : ((1u << S::LPO) - 1u)) << lane0;
+    const unsigned char *featp = static_cast<const unsigned char *>(p.feat) + ol * S::VB;
+    const int share = (P + S::OWNERS - 1) / S::OWNERS;
+    const int beg = active ? min(P, o * share) : P;
+    const int end = active ? min(P, beg + share) : P;
+
+    bool head_cut = false;                         // this owner finishes an interval cut by its share end
+    int head_bev = -1;
+    if (active) {
+        const bool head = beg == 0 || beg >= end || __ldg(p.ranks_bev + T0 + beg - 1) != __ldg(p.ranks_bev + T0 + beg);
+        float acc[S::EPL];
+#pragma unroll
+        for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
+        bool to_slot = !head;                      // the next finished segment continues a previous share
+        // lane ol < BATCH holds the ranks of point v0 + ol: depth / feature
+        // rows for points of the share (-1 otherwise), the cell for points of the chunk
+        auto fetch_idx = [&](int v0, int &ra, int &rb, int &rc) {
+            ra = -1;
+            rb = -1;
+            rc = -1;
+            const int j = v0 + ol;
+            if (ol < S::BATCH && j < P) {
+                rc = __ldg(p.ranks_bev + T0 + j);
+                if (j < end) {
+                    const int x = __ldg(p.ranks_depth + T0 + j);
+                    const int y = __ldg(p.ranks_feat + T0 + j);
+                    if (x >= 0 && x < p.n_depth && y >= 0 && y < p.n_feat_rows) {
+                        ra = x;
+                        rb = y;
+                    }
+                }
+            }
+        };
+        int rd, rf, rc;
+        fetch_idx(beg, rd, rf, rc);
+        for (int v0 = beg; v0 < beg + share; v0 += S::BATCH) {
+            int rd_next, rf_next, rc_next;
+            fetch_idx(v0 + S::BATCH, rd_next, rf_next, rc_next);   // prefetch the next batch's ranks
+            // bit kk of ends: point v0 + kk is the last of its interval
+            const int succ_in = __shfl_sync(gmask, rc, lane0 + min(ol + 1, S::BATCH - 1));
+            const int succ_nx = __shfl_sync(gmask, rc_next, lane0);
+            const int j = v0 + ol;
+            const bool is_end = ol < S::BATCH && j < end &&
+                                (j + 1 == P || rc != (ol + 1 < S::BATCH ? succ_in : succ_nx));
+            const unsigned ends = __ballot_sync(gmask, is_end) >> lane0;
+            int a[S::BATCH], b[S::BATCH];
+#pragma unroll
+            for (int kk = 0; kk < S::BATCH; ++kk) {
+                a[kk] = __shfl_sync(gmask, rd, lane0 + kk);
+                b[kk] = __shfl_sync(gmask, rf, lane0 + kk);
+            }
+            unsigned short d[S::BATCH];
+            RawVec<S::VB> f[S::BATCH];
+#pragma unroll
+            for (int kk = 0; kk < S::BATCH; ++kk) {
+                if (a[kk] >= 0) {
+                    d[kk] = load_depth_h<DT>(p.depth, a[kk]);
+                    f[kk] = load_vec<S::VB>(featp + static_cast<int64_t>(b[kk]) * S::ROWB);
+                } else {                                     // past the share, or an invalid rank: adds +0
+                    d[kk] = 0;
+#pragma unroll
+                    for (int i = 0; i < RawVec<S::VB>::NW; ++i) f[kk].w[i] = 0u;
+                }
+            }
+#pragma unroll
+            for (int kk = 0; kk < S::BATCH; ++kk) {
+                fma_vec<DT, S::VB>(acc, d[kk], f[kk]);
+                if ((ends >> kk) & 1u) {                     // an interval ends with this point
+                    const int bev = __shfl_sync(gmask, rc, lane0 + kk);
+                    if (to_slot) {
+                        float *dst = &sm.slot[0][o][ol * S::EPL];
+#pragma unroll
+                        for (int e = 0; e < S::EPL; ++e) dst[e] = acc[e];
+                        to_slot = false;
+                    } else if (bev >= 0 && bev < p.n_cells) {
+                        store_row_part<S::EPL>(p.out + static_cast<int64_t>(bev) * C + ol * S::EPL, acc, p.scale,
+                                               p.streaming);
+                    }
+#pragma unroll
+                    for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
+                }
+            }
+            rd = rd_next;
+            rf = rf_next;
+            rc = rc_next;
+        }
+        bool cut = false;                                    // the share ends inside an interval
+        if (beg < end && end < P) {
+            head_bev = __ldg(p.ranks_bev + T0 + end - 1);
+            cut = __ldg(p.ranks_bev + T0 + end) == head_bev;
+        }
+        int st = kHead;
+        if (!head) st = to_slot && cut ? kPass : kCont;
+        if (cut) {
+            float *dst = &sm.slot[to_slot ? 0 : 1][o][ol * S::EPL];
+#pragma unroll
+            for (int e = 0; e < S::EPL; ++e) dst[e] = acc[e];
+            head_cut = !to_slot;
+        }
+        if (ol == 0) sm.state[o] = st;
+    }
+
+    // 3. combine cut intervals in owner order (fixed order: deterministic)
+    __syncthreads();
+    if (head_cut) {
+        float acc[S::EPL];
+        const float *src = &sm.slot[1][o][ol * S::EPL];
+#pragma unroll
+        for (int e = 0; e < S::EPL; ++e) acc[e] = src[e];
+        for (int o2 = o + 1; o2 < S::OWNERS; ++o2) {
+            const int st = sm.state[o2];
+            if (st == kHead) break;
+            const float *q = &sm.slot[0][o2][ol * S::EPL];
+#pragma unroll
+            for (int e = 0; e < S::EPL; ++e) acc[e] += q[e];
+            if (st == kCont) break;
+        }
+        if (head_bev >= 0 && head_bev < p.n_cells)
+            store_row_part<S::EPL>(p.out + static_cast<int64_t>(head_bev) * C + ol * S::EPL, acc, p.scale,
+                                   p.streaming);
+    }
+}
+
+// ---------------------------------------------------------------- fill CTA
 
 template <int DT, int C>
 __device__ __forceinline__ void fill_cta(const FwdParams &p, int fidx, FillSmem &sm) {
@@ -514,16 +524,9 @@ template <int DT, int C>
 __global__ void __launch_bounds__(kThreads, BEVPOOL_FWD_MIN_CTAS) k_forward(const FwdParams p) {
     __shared__ __align__(16) FwdSmem<DT, C> sm;
     const int b = blockIdx.x;
-    const int both = 2 * min(p.n_compute, p.n_fill);
-    bool compute;
-    int idx;
-    if (b < both) {
-        compute = (b & 1) == 0;
-        idx = b >> 1;
-    } else {
-        compute = p.n_compute > p.n_fill;
-        idx = (both >> 1) + (b - both);
-    }
+    // compute CTAs (the long ones) first, then fill CTAs in the slots they free
+    const bool compute = b < p.n_compute;
+    const int idx = compute ? b : b - p.n_compute;
     if (compute)
         compute_cta<DT, C>(p, idx, sm.c);
     else
@@ -549,14 +552,16 @@ cudaError_t launch_forward_t(const ForwardArgs &a) {
     p.n_depth = a.n_depth;
     p.scale = a.scale;
     p.streaming = a.streaming_stores;
-    // Chunk size: about one resident wave of compute CTAs, but at least one
-    // interval per owner and at most kMaxChunk.
-    const int64_t slots = static_cast<int64_t>(a.sm_count > 0 ? a.sm_count : 148) * BEVPOOL_FWD_MIN_CTAS;
-    int64_t ipc = div_up(a.n_intervals, slots);
-    if (ipc < S::OWNERS) ipc = S::OWNERS;
-    if (ipc > kMaxChunk) ipc = kMaxChunk;
-    p.ipc = static_cast<int>(ipc);
-    p.n_compute = static_cast<int>(div_up(a.n_intervals, ipc));
+    // About one resident wave of compute CTAs, each with at least a batch of
+    // points per owner; the points per CTA are set on the device from the
+    // actual count.
+    const int64_t slots = static_cast<int64_t>(a.sm_count > 0 ? a.sm_count : 148) *
+                          (a.streaming_stores ? BEVPOOL_FWD_CTAS_PER_SM_DRAM : BEVPOOL_FWD_CTAS_PER_SM_L2);
+    int64_t n_compute = div_up(a.n_points, static_cast<int64_t>(S::OWNERS) * S::BATCH);
+    if (n_compute > slots) n_compute = slots;
+    if (n_compute < 1) n_compute = 1;
+    p.n_compute = static_cast<int>(n_compute);
+    p.n_compute_div = FastDiv(static_cast<uint32_t>(n_compute));
     p.n_fill = static_cast<int>(div_up(a.n_cells, kFillCells));
     p.out = static_cast<__half *>(a.out);
     const int grid = p.n_compute + p.n_fill;

@@ -160,8 +160,8 @@ BEVPOOL_API bevpool_status bevpool_build_map_noalloc(const int32_t *cell_ids, in
  * fp16 (round to nearest even).  Every one of the n_cells rows of `out` is
  * written exactly once; rows no interval names are written as zeros.  No
  * atomics: calls with identical arguments give bit-identical results (the
- * work split, and so the FP32 summation order inside intervals longer than
- * 32 points, depends on n_intervals and the device's SM count).
+ * work split, and so the FP32 summation order inside an interval that two
+ * lane groups share, depends on n_points and the device's SM count).
  *
  *   dtype             BEVPOOL_F16 or BEVPOOL_E4M3 (depth and feat alike).
  *   depth             device, [NC, D, H, W] elements of dtype.
@@ -186,12 +186,14 @@ BEVPOOL_API bevpool_status bevpool_build_map_noalloc(const int32_t *cell_ids, in
  *   out               device, [n_cells, C] fp16, 16-byte aligned; fully
  *                     overwritten.
  *
- * The map is trusted for its ordering (intervals in ascending cell order,
- * one interval per cell).  Indices are still bounds-checked on the device:
- * a point whose ranks_depth / ranks_feat lies outside the tensors
- * contributes nothing, and an interval whose cell lies outside [0, n_cells)
- * or whose range lies outside [0, n_points) is skipped.  Use
- * bevpool_validate_map to check a map.
+ * The map is trusted for its ordering: ranks_bev ascending and the
+ * intervals its maximal runs, as bevpool_build_map writes them (the kernel
+ * splits work at interval starts and ends an interval where ranks_bev
+ * changes).  Indices are still bounds-checked on the device: a point whose
+ * ranks_depth / ranks_feat lies outside the tensors contributes nothing, a
+ * cell outside [0, n_cells) is not written, and nothing outside
+ * [0, n_points) of the map arrays is read.  Use bevpool_validate_map to
+ * check a map.
  */
 BEVPOOL_API bevpool_status bevpool_forward(bevpool_dtype dtype, const void *depth, const void *feat,
                                int32_t NC, int32_t D, int32_t H, int32_t W, int32_t C,
