@@ -63,6 +63,7 @@ def _load():
             lib.oracle_half_array_to_double.argtypes = [vp, i64, vp]
             lib.oracle_half_array_to_double.restype = None
             lib.oracle_e4m3_array_to_double.argtypes = [vp, i64, vp]
+            lib.oracle_double_array_to_e4m3.argtypes = [vp, i64, vp]
             lib.oracle_e4m3_array_to_double.restype = None
             lib.oracle_build_map.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
             lib.oracle_build_map.restype = ctypes.c_int
@@ -89,6 +90,14 @@ def e4m3_to_double(codes: np.ndarray) -> np.ndarray:
     src = np.ascontiguousarray(codes).view(np.uint8)
     out = np.empty(src.shape, dtype=np.float64)
     _load().oracle_e4m3_array_to_double(_ptr(src), src.size, _ptr(out))
+    return out
+
+
+def e4m3_from_double(values: np.ndarray) -> np.ndarray:
+    """Nearest OCP E4M3 codes (round half to even, saturating at +-448, sign kept)."""
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().oracle_double_array_to_e4m3(_ptr(v), v.size, _ptr(out))
     return out
 
 
@@ -141,3 +150,15 @@ def forward(dtype: str, cell_ids: np.ndarray, NC: int, D: int, H: int, W: int, n
     if rc != OK:
         raise OracleError(f"oracle_forward failed with code {rc}")
     return out
+
+
+def forward_e4m3_out(dtype: str, cell_ids: np.ndarray, NC: int, D: int, H: int, W: int, n_cells: int,
+                     C: int, depth: np.ndarray, feat: np.ndarray, depth_scale: float, feat_scale: float,
+                     out_scale: float):
+    """The forward with an E4M3 output: every output value divided by the
+    per-tensor ``out_scale`` and rounded to the nearest E4M3 code.  Returns
+    (codes uint8 [n_cells, C], the exact scaled values float64 [n_cells, C])."""
+    if not (out_scale > 0.0 and np.isfinite(out_scale)):
+        raise OracleError("out_scale must be positive and finite")
+    v = forward(dtype, cell_ids, NC, D, H, W, n_cells, C, depth, feat, depth_scale, feat_scale) / out_scale
+    return e4m3_from_double(v), v

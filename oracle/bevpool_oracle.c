@@ -30,7 +30,12 @@
  *     frustum order by cell), intervals by ascending cell;
  *   - cells no point reaches are 0 in the output;
  *   - FP8 inputs are OCP E4M3 codes with one scale per tensor; the value the
- *     method sees is code_value * scale.
+ *     method sees is code_value * scale;
+ *   - the FP8 output (section "Eliminate redundant scatter traffic", Figure
+ *     4: the FP8 path halves output bytes too; section "Map the algorithm to
+ *     hardware": the NVFP4 experiment keeps depth and output in FP8) is the
+ *     E4M3 code nearest to value / out_scale, out_scale being one per-tensor
+ *     scale the caller chooses; ties to even, saturated at +-448.
  *
  * The forward oracle does NOT go through the scatter map: it walks the
  * frustum points in their original order, so it also checks the map.
@@ -92,6 +97,49 @@ void oracle_e4m3_array_to_double(const uint8_t *src, int64_t n, double *dst)
 {
     for (int64_t i = 0; i < n; ++i)
         dst[i] = oracle_e4m3_to_double(src[i]);
+}
+
+/* Nearest OCP E4M3 code to x: round half to even, magnitudes above the
+ * largest finite value (448) saturate to it, the sign is kept (a negative
+ * value that rounds to zero gives -0).  Written from the format itself: the
+ * representable values between 2^e and 2^(e+1) are spaced 2^(e-3) apart for
+ * e >= -6, and the subnormals 2^-9 apart below 2^-6. */
+uint8_t oracle_e4m3_from_double(double x)
+{
+    if (isnan(x))
+        return 0x7f;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    double step;
+    if (a < ldexp(1.0, -6)) {
+        step = ldexp(1.0, -9);
+    } else {
+        int k;
+        frexp(a, &k);                    /* a = f * 2^k, f in [0.5, 1): 2^(k-1) <= a < 2^k */
+        step = ldexp(1.0, k - 1 - 3);
+    }
+    double v = rint(a / step) * step;    /* default rounding mode: half to even */
+    if (v > 448.0)
+        v = 448.0;
+    if (v == 0.0)
+        return sign;
+    int k;
+    frexp(v, &k);
+    int e = k - 1;                       /* 2^e <= v < 2^(e+1) */
+    uint8_t code;
+    if (e < -6)
+        code = (uint8_t)(v / ldexp(1.0, -9));                 /* subnormal: mantissa only */
+    else
+        code = (uint8_t)(((e + 7) << 3) | ((int)(v / ldexp(1.0, e - 3)) - 8));
+    return sign | code;
+}
+
+void oracle_double_array_to_e4m3(const double *src, int64_t n, uint8_t *dst)
+{
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = oracle_e4m3_from_double(src[i]);
 }
 
 typedef struct {

@@ -190,3 +190,27 @@ def test_pins_catch_planted_mistakes():
     plants.append(wrong_row)
     for bad in plants:
         assert check_forward_pins(bad, wl) != []
+
+
+def test_e4m3_output_closed_form():
+    """E4M3 output with out_scale 0.5 of all-ones inputs: the codes decode to
+    exactly 2 x the per-cell point count (even integers up to 32 are E4M3
+    values), and untouched cells are the zero code."""
+    NC, D, H, W, C, cells = 2, 3, 4, 5, 16, 40
+    rng = np.random.default_rng(17)
+    cid = rng.integers(-1, cells, size=NC * D * H * W).astype(np.int32)
+    wl = workloads.custom(NC, D, H, W, C, cells, cid, depth=np.ones((NC, D, H, W), np.float16),
+                          feat=np.ones((NC, H, W, C), np.float16))
+    codes, v = oracle.forward_e4m3_out("f16", wl.cell_ids, *wl.dims(), wl.n_cells, C, wl.depth, wl.feat,
+                                       1.0, 1.0, 0.5)
+    count = np.bincount(cid[cid >= 0], minlength=cells).astype(np.float64)
+    assert count.max() <= 16
+    assert np.array_equal(oracle.e4m3_to_double(codes), np.repeat(2 * count[:, None], C, axis=1))
+    assert np.array_equal(v, np.repeat(2 * count[:, None], C, axis=1))
+
+
+def test_e4m3_output_rejects_bad_scale():
+    wl = workloads.tiny()
+    with pytest.raises(oracle.OracleError):
+        oracle.forward_e4m3_out(wl.dtype, wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat,
+                                1.0, 1.0, 0.0)
