@@ -40,7 +40,8 @@ if ROOT not in sys.path:
 METRIC = "BEV-pool forward µs/call and GB/s vs L2/HBM roofline (209K pts, C=80, FP16/FP8)"
 FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
-FORWARD_SOURCES = ["forward_impl.cuh", "forward_f16.cu", "forward_e4m3.cu", "bevpool_internal.cuh"]
+FORWARD_SOURCES = ["forward_impl.cuh", "forward_f16.cu", "forward_e4m3.cu", "forward_f16_e4m3out.cu",
+                   "forward_e4m3_e4m3out.cu", "bevpool_internal.cuh"]
 
 
 def forward_source_hash() -> str:
@@ -76,7 +77,7 @@ def recorded_traffic(workload: str):
     return None
 
 
-def bytes_model(wl, n_points: int, n_intervals: int) -> dict:
+def bytes_model(wl, n_points: int, n_intervals: int, out_bytes: int = 2) -> dict:
     """Bytes one forward must move.  'footprint' = every array the forward
     touches, once (the compulsory HBM traffic after an L2 flush);
     'gather' = what the owners actually read per point (L2-level)."""
@@ -85,7 +86,7 @@ def bytes_model(wl, n_points: int, n_intervals: int) -> dict:
     iv = 8 * n_intervals                 # interval_starts, interval_lengths
     depth = wl.n_frustum * eb
     feat = wl.n_feat_rows * wl.C * eb
-    out = wl.n_cells * wl.C * 2
+    out = wl.n_cells * wl.C * out_bytes
     footprint = idx + iv + depth + feat + out
     gather = idx + iv + n_points * eb + n_points * wl.C * eb + out
     return dict(index=idx, intervals=iv, depth=depth, feat=feat, out=out, footprint=footprint, gather=gather)
@@ -174,26 +175,39 @@ def max_over_ranks(values, world: int, device):
     return t.tolist()
 
 
-def config_dict(wl, n_pts: int, n_int: int, world: int) -> dict:
-    return {"workload": f"{wl.name}: NC={wl.NC} D={wl.D} H={wl.H} W={wl.W} C={wl.C} grid={wl.grid} "
-                        f"points={n_pts} intervals={n_int}",
-            "l2": "flushed (256 MiB written) before the map build and before the forward",
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+def config_dict(wl, n_pts: int, n_int: int, world: int, out_dtype: str = "f16") -> dict:
+    d = {"workload": f"{wl.name}: NC={wl.NC} D={wl.D} H={wl.H} W={wl.W} C={wl.C} grid={wl.grid} "
+                     f"points={n_pts} intervals={n_int}",
+         "l2": "flushed (256 MiB written) before the map build and before the forward",
+         "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    if out_dtype == "e4m3":
+        d["output"] = "E4M3 codes of value / out_scale, out_scale = max|output| / 448 (calibrated once, untimed)"
+    return d
 
 
-def cpu_oracle_time(wl, budget_s: float = 10.0, max_reps: int = 50) -> dict:
+def oracle_call(wl, out_scale=None):
+    """One oracle forward of the workload (with the E4M3 output when out_scale is given)."""
+    import oracle
+
+    if out_scale is None:
+        return lambda: oracle.forward(wl.dtype, wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat,
+                                      wl.depth_scale, wl.feat_scale)
+    return lambda: oracle.forward_e4m3_out(wl.dtype, wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat,
+                                           wl.depth_scale, wl.feat_scale, out_scale)
+
+
+def cpu_oracle_time(wl, budget_s: float = 10.0, max_reps: int = 50, out_scale=None) -> dict:
     """Times the oracle's forward on the full workload, single-threaded."""
     import oracle
 
     oracle.build()
-    oracle.forward(wl.dtype, wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat,
-                   wl.depth_scale, wl.feat_scale)       # load + page in
+    call = oracle_call(wl, out_scale)
+    call()                                              # load + page in
     times = []
     t_start = time.perf_counter()
     while len(times) < max_reps and (time.perf_counter() - t_start < budget_s or len(times) < 3):
         t0 = time.perf_counter()
-        oracle.forward(wl.dtype, wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat,
-                       wl.depth_scale, wl.feat_scale)
+        call()
         times.append(time.perf_counter() - t0)
     return {"value": statistics.mean(times) * 1e6, "unit": "us/call", "cores": 1, "kind": "oracle",
             "sample": f"full {wl.name} workload ({wl.n_kept} points, C={wl.C}), {len(times)} calls of the "
@@ -210,8 +224,12 @@ def run_reference(args) -> None:
     wl = workloads.make(args.config)
     oracle.build()
     m = oracle.build_map(wl.cell_ids, *wl.dims(), wl.n_cells)
-    call = lambda: oracle.forward(wl.dtype, wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat,
-                                  wl.depth_scale, wl.feat_scale)
+    out_scale = None
+    if args.out_dtype == "e4m3":                        # the same calibration as the GPU arm: max|output| / 448
+        ref = oracle.forward(wl.dtype, wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat,
+                             wl.depth_scale, wl.feat_scale)
+        out_scale = float(np.abs(ref).max()) / 448.0 or 1.0
+    call = oracle_call(wl, out_scale)
     for _ in range(args.warmup):
         call()
     times = []
@@ -223,7 +241,7 @@ def run_reference(args) -> None:
     line = {"metric": METRIC, "value": v, "unit": "us/call", "impl": "reference", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_dict(wl, m["n_points"], m["n_intervals"], world),
+            "config": config_dict(wl, m["n_points"], m["n_intervals"], world, args.out_dtype),
             "cpu_baseline": {"value": v, "unit": "us/call", "cores": 1, "kind": "oracle",
                              "sample": f"each step one full {wl.name} forward of the single-threaded FP64 C oracle"},
             "e2e": {"value": v, "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -257,13 +275,20 @@ def run_ours(args) -> None:
     bevpool.build_map(cells, *wl.dims(), wl.n_cells, out=m, workspace=ws, sync=True)
     n_pts, n_int = m.n_points, m.n_intervals
     cap = (n_pts, n_int)
-    out = torch.empty((wl.n_cells, wl.C), dtype=torch.float16, device=device)
+    e4m3_out = args.out_dtype == "e4m3"
+    out_scale = None
+    if e4m3_out:                                        # calibration (untimed): max|output| / 448
+        probe = bevpool.forward(m, depth, feat, wl.C, dtype=dt, depth_scale=wl.depth_scale,
+                                feat_scale=wl.feat_scale, capacity=cap)
+        out_scale = float(probe.float().abs().max().item()) / 448.0 or 1.0
+        del probe
+    out = torch.empty((wl.n_cells, wl.C), dtype=torch.uint8 if e4m3_out else torch.float16, device=device)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
 
     def fwd(o=out):
         bevpool.forward(m, depth, feat, wl.C, dtype=dt, depth_scale=wl.depth_scale, feat_scale=wl.feat_scale,
-                        out=o, capacity=cap)
+                        out=o, capacity=cap, out_scale=out_scale)
 
     def build():
         bevpool.build_map(cells, *wl.dims(), wl.n_cells, out=m, workspace=ws, sync=False)
@@ -338,7 +363,7 @@ def run_ours(args) -> None:
         warm_us = f"unavailable: {type(e).__name__}"
 
     # End to end through the C ABI from pinned host buffers.
-    out_h = torch.empty((wl.n_cells, wl.C), dtype=torch.float16).pin_memory()
+    out_h = torch.empty((wl.n_cells, wl.C), dtype=out.dtype).pin_memory()
     e2e_steps = min(args.steps, 200)
     e2e_ms = []
     for i in range(e2e_steps + 3):
@@ -359,7 +384,8 @@ def run_ours(args) -> None:
 
     if rank != 0:
         return
-    bm = bytes_model(wl, n_pts, n_int)
+    bm = bytes_model(wl, n_pts, n_int, 1 if e4m3_out else 2)
+    traffic_key = wl.name + ("_e4m3out" if e4m3_out else "")
     peak, peak_kind = measured_peaks()
     fwd_s = fwd_mean / 1e3
     achieved = bm["footprint"] / fwd_s / 1e9
@@ -374,14 +400,15 @@ def run_ours(args) -> None:
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": wl.dtype,
+        "dtype": wl.dtype + ("->e4m3" if e4m3_out else ""),
         "data": "synthetic (seeded generator shaped like the pages' workload; nuScenes not used)",
-        "config": config_dict(wl, n_pts, n_int, world),
+        "config": config_dict(wl, n_pts, n_int, world, args.out_dtype),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": recorded_traffic(wl.name),
+                     "frac": achieved / peak, "traffic": recorded_traffic(traffic_key),
                      "kernel": "k_forward", "bytes_per_launch": bm["footprint"],
                      "peak_source": f"hbm_gbs of MEASURED_PEAKS.json ({peak_kind})"},
-        "cpu_baseline": cpu_oracle_time(wl) if (world == 1 and not args.no_cpu_baseline) else None,
+        "cpu_baseline": (cpu_oracle_time(wl, out_scale=out_scale)
+                         if (world == 1 and not args.no_cpu_baseline) else None),
         "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clocks,
@@ -410,6 +437,8 @@ def main():
     ap.add_argument("--config", default="canonical",
                     choices=["tiny", "canonical", "canonical_fp8", "bevdet", "dram_batch"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--out-dtype", choices=["f16", "e4m3"], default="f16",
+                    help="output of the forward: fp16, or E4M3 codes (bevpool_forward_e4m3_out)")
     args = ap.parse_args()
     if args.impl == "reference":
         if args.steps > 100:

@@ -58,6 +58,9 @@ _lib.bevpool_build_map_noalloc.restype = ctypes.c_int
 _lib.bevpool_forward.argtypes = [ctypes.c_int, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _f32,
                                  _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp]
 _lib.bevpool_forward.restype = ctypes.c_int
+_lib.bevpool_forward_e4m3_out.argtypes = [ctypes.c_int, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _f32,
+                                          _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp]
+_lib.bevpool_forward_e4m3_out.restype = ctypes.c_int
 _lib.bevpool_validate_map.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]
 _lib.bevpool_validate_map.restype = ctypes.c_int
 
@@ -118,6 +121,16 @@ def bevpool_forward(dtype: int, depth: int, feat: int, NC: int, D: int, H: int, 
     return _lib.bevpool_forward(dtype, depth, feat, NC, D, H, W, C, depth_scale, feat_scale, ranks_depth,
                                 ranks_feat, ranks_bev, interval_starts, interval_lengths, n_points, n_intervals,
                                 d_counts, n_cells, out, stream)
+
+
+def bevpool_forward_e4m3_out(dtype: int, depth: int, feat: int, NC: int, D: int, H: int, W: int, C: int,
+                             depth_scale: float, feat_scale: float, out_scale: float, ranks_depth: int,
+                             ranks_feat: int, ranks_bev: int, interval_starts: int, interval_lengths: int,
+                             n_points: int, n_intervals: int, d_counts: Optional[int], n_cells: int, out: int,
+                             stream: int) -> int:
+    return _lib.bevpool_forward_e4m3_out(dtype, depth, feat, NC, D, H, W, C, depth_scale, feat_scale, out_scale,
+                                         ranks_depth, ranks_feat, ranks_bev, interval_starts, interval_lengths,
+                                         n_points, n_intervals, d_counts, n_cells, out, stream)
 
 
 def bevpool_validate_map(ranks_depth: int, ranks_feat: int, ranks_bev: int, interval_starts: int,
@@ -206,27 +219,37 @@ def build_map(cell_ids, NC: int, D: int, H: int, W: int, n_cells: int, *, out: O
 
 
 def forward(m: ScatterMap, depth, feat, C: int, *, dtype: int = BEVPOOL_F16, depth_scale: float = 1.0,
-            feat_scale: float = 1.0, out=None, stream=None, capacity: Optional[tuple] = None):
-    """bevpool_forward over a map.  Returns the fp16 [n_cells, C] output tensor.
+            feat_scale: float = 1.0, out=None, stream=None, capacity: Optional[tuple] = None,
+            out_scale: Optional[float] = None):
+    """bevpool_forward over a map.  Returns the [n_cells, C] output tensor:
+    fp16, or, when ``out_scale`` is given, uint8 E4M3 codes of value / out_scale
+    (bevpool_forward_e4m3_out).
 
     If the map's host counts are unknown (built with sync=False), the device
     counts are used with ``capacity`` = (max points, max intervals) as bounds."""
     import torch
 
     if out is None:
-        out = torch.empty((m.n_cells, C), dtype=torch.float16, device=feat.device)
+        out = torch.empty((m.n_cells, C), dtype=torch.float16 if out_scale is None else torch.uint8,
+                          device=feat.device)
     if m.n_points is not None and capacity is None:
         n_pts, n_int, dc = m.n_points, m.n_intervals, None
     else:
         nf = m.NC * m.D * m.H * m.W
         n_pts, n_int = capacity if capacity is not None else (nf, min(nf, m.n_cells))
         dc = m.d_counts.data_ptr()
-    st = bevpool_forward(dtype, depth.data_ptr(), feat.data_ptr(), m.NC, m.D, m.H, m.W, C, depth_scale, feat_scale,
-                         m.ranks_depth.data_ptr(), m.ranks_feat.data_ptr(), m.ranks_bev.data_ptr(),
-                         m.interval_starts.data_ptr(), m.interval_lengths.data_ptr(), n_pts, n_int, dc, m.n_cells,
-                         out.data_ptr(), _stream(stream))
-    if st != BEVPOOL_OK:
-        raise BevpoolError(st, "bevpool_forward")
+    maps = (m.ranks_depth.data_ptr(), m.ranks_feat.data_ptr(), m.ranks_bev.data_ptr(), m.interval_starts.data_ptr(),
+            m.interval_lengths.data_ptr(), n_pts, n_int, dc, m.n_cells, out.data_ptr(), _stream(stream))
+    if out_scale is None:
+        st = bevpool_forward(dtype, depth.data_ptr(), feat.data_ptr(), m.NC, m.D, m.H, m.W, C, depth_scale,
+                             feat_scale, *maps)
+        if st != BEVPOOL_OK:
+            raise BevpoolError(st, "bevpool_forward")
+    else:
+        st = bevpool_forward_e4m3_out(dtype, depth.data_ptr(), feat.data_ptr(), m.NC, m.D, m.H, m.W, C, depth_scale,
+                                      feat_scale, out_scale, *maps)
+        if st != BEVPOOL_OK:
+            raise BevpoolError(st, "bevpool_forward_e4m3_out")
     return out
 
 

@@ -196,14 +196,19 @@ bevpool_status bevpool_build_map(const int32_t *cell_ids, int32_t NC, int32_t D,
     return h_counts[2] > 0 ? BEVPOOL_ERR_OUT_OF_RANGE : BEVPOOL_OK;
 }
 
-bevpool_status bevpool_forward(bevpool_dtype dtype, const void *depth, const void *feat, int32_t NC, int32_t D,
-                               int32_t H, int32_t W, int32_t C, float depth_scale, float feat_scale,
-                               const int32_t *ranks_depth, const int32_t *ranks_feat, const int32_t *ranks_bev,
-                               const int32_t *interval_starts, const int32_t *interval_lengths,
-                               int32_t n_points, int32_t n_intervals, const int32_t *d_counts, int32_t n_cells,
-                               void *out, void *stream) {
+namespace {
+
+// Shared body of the two forward entry points (fp16 output, or E4M3 output
+// codes of value / out_scale).
+bevpool_status forward_impl(bevpool_dtype dtype, const void *depth, const void *feat, int32_t NC, int32_t D,
+                            int32_t H, int32_t W, int32_t C, float depth_scale, float feat_scale, bool e4m3_out,
+                            float out_scale, const int32_t *ranks_depth, const int32_t *ranks_feat,
+                            const int32_t *ranks_bev, const int32_t *interval_starts,
+                            const int32_t *interval_lengths, int32_t n_points, int32_t n_intervals,
+                            const int32_t *d_counts, int32_t n_cells, void *out, void *stream) {
     if (dtype != BEVPOOL_F16 && dtype != BEVPOOL_E4M3) return BEVPOOL_ERR_UNSUPPORTED;
     if (!forward_supported(static_cast<int>(dtype), C)) return BEVPOOL_ERR_UNSUPPORTED;
+    if (e4m3_out && C % 16 != 0) return BEVPOOL_ERR_UNSUPPORTED;
     if (!frustum_ok(NC, D, H, W) || n_cells < 1) return BEVPOOL_ERR_INVALID_ARG;
     if (static_cast<int64_t>(n_cells) * C > INT32_MAX) return BEVPOOL_ERR_INVALID_ARG;
     const int64_t nf = static_cast<int64_t>(NC) * D * H * W;
@@ -216,7 +221,9 @@ bevpool_status bevpool_forward(bevpool_dtype dtype, const void *depth, const voi
     const void *idx[] = {ranks_depth, ranks_feat, ranks_bev, interval_starts, interval_lengths, d_counts};
     for (const void *p : idx)
         if (p && !aligned(p, 4)) return BEVPOOL_ERR_INVALID_ARG;
-    const float scale = depth_scale * feat_scale;
+    if (e4m3_out && !(std::isfinite(out_scale) && out_scale > 0.0f)) return BEVPOOL_ERR_INVALID_ARG;
+    float scale = depth_scale * feat_scale;
+    if (e4m3_out) scale /= out_scale;
     if (!std::isfinite(scale)) return BEVPOOL_ERR_INVALID_ARG;
 
     DeviceInfo info;
@@ -238,18 +245,49 @@ bevpool_status bevpool_forward(bevpool_dtype dtype, const void *depth, const voi
     a.n_depth = nf;
     a.n_feat_rows = NC * H * W;
     a.scale = scale;
+    a.out_e4m3 = e4m3_out ? 1 : 0;
     // Memory regime (section "Classify the memory regime"): when the bytes the
     // forward touches do not fit comfortably in L2, stream the output past it.
     const int64_t eb = dtype == BEVPOOL_F16 ? 2 : 1;
+    const int64_t ob = e4m3_out ? 1 : 2;
     const int64_t footprint = static_cast<int64_t>(n_points) * 12 + static_cast<int64_t>(n_intervals) * 8 +
                               nf * eb + static_cast<int64_t>(a.n_feat_rows) * C * eb +
-                              static_cast<int64_t>(n_cells) * C * 2;
+                              static_cast<int64_t>(n_cells) * C * ob;
     a.streaming_stores = footprint > static_cast<int64_t>(info.l2_bytes) / 2 ? 1 : 0;
     a.sm_count = info.sm_count;
     a.out = out;
     a.stream = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = dtype == BEVPOOL_F16 ? launch_forward_f16(a) : launch_forward_e4m3(a);
+    cudaError_t e;
+    if (e4m3_out)
+        e = dtype == BEVPOOL_F16 ? launch_forward_f16_e4m3out(a) : launch_forward_e4m3_e4m3out(a);
+    else
+        e = dtype == BEVPOOL_F16 ? launch_forward_f16(a) : launch_forward_e4m3(a);
     return cuda_status(e);
+}
+
+}  // namespace
+
+bevpool_status bevpool_forward(bevpool_dtype dtype, const void *depth, const void *feat, int32_t NC, int32_t D,
+                               int32_t H, int32_t W, int32_t C, float depth_scale, float feat_scale,
+                               const int32_t *ranks_depth, const int32_t *ranks_feat, const int32_t *ranks_bev,
+                               const int32_t *interval_starts, const int32_t *interval_lengths,
+                               int32_t n_points, int32_t n_intervals, const int32_t *d_counts, int32_t n_cells,
+                               void *out, void *stream) {
+    return forward_impl(dtype, depth, feat, NC, D, H, W, C, depth_scale, feat_scale, false, 0.0f, ranks_depth,
+                        ranks_feat, ranks_bev, interval_starts, interval_lengths, n_points, n_intervals, d_counts,
+                        n_cells, out, stream);
+}
+
+bevpool_status bevpool_forward_e4m3_out(bevpool_dtype dtype, const void *depth, const void *feat, int32_t NC,
+                                        int32_t D, int32_t H, int32_t W, int32_t C, float depth_scale,
+                                        float feat_scale, float out_scale, const int32_t *ranks_depth,
+                                        const int32_t *ranks_feat, const int32_t *ranks_bev,
+                                        const int32_t *interval_starts, const int32_t *interval_lengths,
+                                        int32_t n_points, int32_t n_intervals, const int32_t *d_counts,
+                                        int32_t n_cells, void *out, void *stream) {
+    return forward_impl(dtype, depth, feat, NC, D, H, W, C, depth_scale, feat_scale, true, out_scale, ranks_depth,
+                        ranks_feat, ranks_bev, interval_starts, interval_lengths, n_points, n_intervals, d_counts,
+                        n_cells, out, stream);
 }
 
 bevpool_status bevpool_validate_map(const int32_t *ranks_depth, const int32_t *ranks_feat, const int32_t *ranks_bev,

@@ -129,15 +129,18 @@ struct ForwardArgs {
     int32_t n_points, n_intervals, n_cells, C;
     int64_t n_depth;          // NC*D*H*W
     int32_t n_feat_rows;      // NC*H*W
-    float scale;              // depth_scale * feat_scale
+    float scale;              // depth_scale * feat_scale (/ out_scale for an E4M3 output)
+    int out_e4m3;             // 1: E4M3 output codes, 0: fp16 output
     int streaming_stores;     // 1: evict-first output stores (HBM regime)
     int sm_count;             // SMs of the current device (launch sizing)
     void *out;
     cudaStream_t stream;
 };
 bool forward_supported(int dtype, int C);
-cudaError_t launch_forward_f16(const ForwardArgs &a);
+cudaError_t launch_forward_f16(const ForwardArgs &a);             // fp16 output
 cudaError_t launch_forward_e4m3(const ForwardArgs &a);
+cudaError_t launch_forward_f16_e4m3out(const ForwardArgs &a);     // E4M3 output (C % 16 == 0)
+cudaError_t launch_forward_e4m3_e4m3out(const ForwardArgs &a);
 
 // Map validation (abi.cu).
 cudaError_t launch_validate_map(const int32_t *ranks_depth, const int32_t *ranks_feat,

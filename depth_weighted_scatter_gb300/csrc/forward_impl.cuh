@@ -26,7 +26,7 @@
 //                after a barrier the owner that started it adds them in owner
 //                order, so the sum order is fixed and the result deterministic.
 //
-//   fill CTA     owns a tile of kFillCells consecutive cells.  It finds the
+//   fill CTA     owns a tile of 256-1024 consecutive cells.  It finds the
 //                tile's points in the sorted ranks_bev with a CTA-wide k-ary
 //                search (2-3 dependent loads), marks the cells that have
 //                points, and writes zeros to the rest with 16-byte stores.
@@ -60,7 +60,10 @@ namespace bevpool {
 
 constexpr int kDtypeF16 = 0;
 constexpr int kDtypeE4M3 = 1;
-constexpr int kFillCells = 256;
+constexpr int kOutF16 = 0;     // output element: fp16 (round to nearest even)
+constexpr int kOutE4M3 = 1;    // output element: OCP E4M3 code (round to nearest even, saturating)
+constexpr int kFillCellsMin = 256;    // cells per fill CTA: a power of two in [min, max], chosen per call
+constexpr int kFillCellsMax = 1024;
 // Compute CTAs per SM (one wave of them): with the output resident in L2,
 // two, leaving a slot for fill CTAs to run alongside; when the output streams
 // to DRAM, three (the gathers need the issue slots more than the fills).
@@ -84,7 +87,6 @@ struct FwdShape {
     static constexpr int OWNERS = kWarps * OPW;                 // owners per CTA
     static constexpr int BATCH_CFG = VB >= 32 ? 4 : ((DT == kDtypeF16 || VB < 16) ? BEVPOOL_FWD_BATCH : 4);
     static constexpr int BATCH = BATCH_CFG < LPO ? BATCH_CFG : LPO;   // points in flight per owner (<= LPO)
-    static constexpr int OUT_VECS = C * 2 / 16;                 // 16-byte fp16 vectors per out row
     static_assert(ROWB % VB == 0 && (VB == 2 || VB == 4 || VB == 8 || VB == 16 || VB == 32), "bad vector width");
     static_assert(LPO >= 4 && LPO <= 32, "bad lane mapping");
     static_assert(C % 8 == 0, "C must be a multiple of 8");
@@ -109,7 +111,8 @@ struct FwdParams {
     int n_compute;                // compute CTAs
     FastDiv n_compute_div;        // division by n_compute
     int n_fill;                   // fill CTAs
-    __half *out;
+    int fill_cells;               // cells per fill CTA
+    unsigned char *out;           // [n_cells, C] elements of the output type
 };
 
 // ---------------------------------------------------------------- element access
@@ -219,27 +222,52 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// Store EPL channels (scaled, rounded to fp16) at dst (2*EPL bytes, aligned).
-template <int EPL>
-__device__ __forceinline__ void store_row_part(__half *dst, const float *acc, float scale, bool streaming) {
-    constexpr int NW = EPL / 2;   // 32-bit words
-    uint32_t w[NW];
+template <typename V>
+__device__ __forceinline__ void store_vec(V *p, const V &v, bool streaming) {
+    if (streaming) __stcs(p, v); else *p = v;
+}
+
+// Store EPL channels, scaled and rounded to the output type, at dst
+// (EPL * element bytes, aligned to that size).
+template <int OT, int EPL>
+__device__ __forceinline__ void store_row_part(unsigned char *dst, const float *acc, float scale, bool streaming) {
+    if constexpr (OT == kOutF16) {
+        constexpr int NW = EPL / 2;   // 32-bit words
+        uint32_t w[NW];
 #pragma unroll
-    for (int i = 0; i < NW; ++i) w[i] = pack_half2(acc[2 * i] * scale, acc[2 * i + 1] * scale);
-    if constexpr (NW % 4 == 0) {
+        for (int i = 0; i < NW; ++i) w[i] = pack_half2(acc[2 * i] * scale, acc[2 * i + 1] * scale);
+        if constexpr (NW % 4 == 0) {
 #pragma unroll
-        for (int q = 0; q < NW / 4; ++q) {
-            const uint4 v = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-            uint4 *p = reinterpret_cast<uint4 *>(dst) + q;
-            if (streaming) __stcs(p, v); else *p = v;
+            for (int q = 0; q < NW / 4; ++q)
+                store_vec(reinterpret_cast<uint4 *>(dst) + q, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]),
+                          streaming);
+        } else if constexpr (NW == 2) {
+            store_vec(reinterpret_cast<uint2 *>(dst), make_uint2(w[0], w[1]), streaming);
+        } else {
+            store_vec(reinterpret_cast<unsigned int *>(dst), w[0], streaming);
         }
-    } else if constexpr (NW == 2) {
-        const uint2 v = make_uint2(w[0], w[1]);
-        uint2 *p = reinterpret_cast<uint2 *>(dst);
-        if (streaming) __stcs(p, v); else *p = v;
     } else {
-        unsigned int *p = reinterpret_cast<unsigned int *>(dst);
-        if (streaming) __stcs(p, w[0]); else *p = w[0];
+        static_assert(EPL % 4 == 0, "E4M3 rows are stored four codes at a time");
+        constexpr int NW = EPL / 4;   // 32-bit words of four codes
+        uint32_t w[NW];
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+            const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                make_float2(acc[4 * i] * scale, acc[4 * i + 1] * scale), __NV_SATFINITE, __NV_E4M3);
+            const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                make_float2(acc[4 * i + 2] * scale, acc[4 * i + 3] * scale), __NV_SATFINITE, __NV_E4M3);
+            w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+        }
+        if constexpr (NW % 4 == 0) {
+#pragma unroll
+            for (int q = 0; q < NW / 4; ++q)
+                store_vec(reinterpret_cast<uint4 *>(dst) + q, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]),
+                          streaming);
+        } else if constexpr (NW == 2) {
+            store_vec(reinterpret_cast<uint2 *>(dst), make_uint2(w[0], w[1]), streaming);
+        } else {
+            store_vec(reinterpret_cast<unsigned int *>(dst), w[0], streaming);
+        }
     }
 }
 
@@ -258,7 +286,7 @@ constexpr int kCont = 1;   // inside an interval that ends within the share: its
 constexpr int kPass = 2;   // inside an interval that runs through the whole share: its partial is in slot[0]
 
 struct FillSmem {
-    unsigned mark[kFillCells / 32];
+    unsigned mark[kFillCellsMax / 32];
 };
 
 template <int DT, int C>
@@ -328,9 +356,10 @@ __device__ __forceinline__ void cta_next_starts(const FwdParams &p, int n, int n
     *t1 = min(max(r1, *t0), n);
 }
 
-template <int DT, int C>
+template <int DT, int C, int OT>
 __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, ComputeSmem<DT, C> &sm) {
     using S = FwdShape<DT, C>;
+    constexpr int OB = OT == kOutF16 ? 2 : 1;      // output bytes per element
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
     __shared__ int s_bounds[2];
@@ -438,8 +467,8 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
                         for (int e = 0; e < S::EPL; ++e) dst[e] = acc[e];
                         to_slot = false;
                     } else if (bev >= 0 && bev < p.n_cells) {
-                        store_row_part<S::EPL>(p.out + static_cast<int64_t>(bev) * C + ol * S::EPL, acc, p.scale,
-                                               p.streaming);
+                        store_row_part<OT, S::EPL>(p.out + (static_cast<int64_t>(bev) * C + ol * S::EPL) * OB, acc,
+                                                   p.scale, p.streaming);
                     }
 #pragma unroll
                     for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
@@ -481,34 +510,35 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
             if (st == kCont) break;
         }
         if (head_bev >= 0 && head_bev < p.n_cells)
-            store_row_part<S::EPL>(p.out + static_cast<int64_t>(head_bev) * C + ol * S::EPL, acc, p.scale,
-                                   p.streaming);
+            store_row_part<OT, S::EPL>(p.out + (static_cast<int64_t>(head_bev) * C + ol * S::EPL) * OB, acc,
+                                       p.scale, p.streaming);
     }
 }
 
 // ---------------------------------------------------------------- fill CTA
 
-template <int DT, int C>
+template <int DT, int C, int OT>
 __device__ __forceinline__ void fill_cta(const FwdParams &p, int fidx, FillSmem &sm) {
-    using S = FwdShape<DT, C>;
     int n_pts = p.n_points;
     if (p.d_counts) n_pts = min(n_pts, __ldg(p.d_counts + 0));
     if (n_pts < 0) n_pts = 0;
-    const int c0 = fidx * kFillCells;
-    const int c1 = min(c0 + kFillCells, p.n_cells);
-    if (threadIdx.x < kFillCells / 32) sm.mark[threadIdx.x] = 0u;
+    const int c0 = fidx * p.fill_cells;
+    const int c1 = min(c0 + p.fill_cells, p.n_cells);
+    if (threadIdx.x < kFillCellsMax / 32) sm.mark[threadIdx.x] = 0u;
     int t0, t1;
     cta_lower_bound2(p.ranks_bev, n_pts, c0, c1, &t0, &t1);   // contains barriers
     for (int t = t0 + threadIdx.x; t < t1; t += kThreads) {
         const int cell = __ldg(p.ranks_bev + t) - c0;
-        if (cell >= 0 && cell < kFillCells) atomicOr(&sm.mark[cell >> 5], 1u << (cell & 31));
+        if (cell >= 0 && cell < p.fill_cells) atomicOr(&sm.mark[cell >> 5], 1u << (cell & 31));
     }
     __syncthreads();
-    const int total = (c1 - c0) * S::OUT_VECS;
-    uint4 *out = reinterpret_cast<uint4 *>(p.out + static_cast<int64_t>(c0) * C);
+    constexpr int OUT_VECS = C * (OT == kOutF16 ? 2 : 1) / 16;    // 16-byte vectors per output row
+    static_assert(OUT_VECS * 16 == C * (OT == kOutF16 ? 2 : 1), "output rows are whole 16-byte vectors");
+    const int total = (c1 - c0) * OUT_VECS;
+    uint4 *out = reinterpret_cast<uint4 *>(p.out + static_cast<int64_t>(c0) * OUT_VECS * 16);
     const uint4 z = make_uint4(0, 0, 0, 0);
     for (int v = threadIdx.x; v < total; v += kThreads) {
-        const int cell = v / S::OUT_VECS;
+        const int cell = v / OUT_VECS;
         if (!((sm.mark[cell >> 5] >> (cell & 31)) & 1u)) {
             if (p.streaming)
                 __stcs(out + v, z);
@@ -520,7 +550,7 @@ __device__ __forceinline__ void fill_cta(const FwdParams &p, int fidx, FillSmem 
 
 // ---------------------------------------------------------------- kernel
 
-template <int DT, int C>
+template <int DT, int C, int OT>
 __global__ void __launch_bounds__(kThreads, BEVPOOL_FWD_MIN_CTAS) k_forward(const FwdParams p) {
     __shared__ __align__(16) FwdSmem<DT, C> sm;
     const int b = blockIdx.x;
@@ -528,12 +558,12 @@ __global__ void __launch_bounds__(kThreads, BEVPOOL_FWD_MIN_CTAS) k_forward(cons
     const bool compute = b < p.n_compute;
     const int idx = compute ? b : b - p.n_compute;
     if (compute)
-        compute_cta<DT, C>(p, idx, sm.c);
+        compute_cta<DT, C, OT>(p, idx, sm.c);
     else
-        fill_cta<DT, C>(p, idx, sm.f);
+        fill_cta<DT, C, OT>(p, idx, sm.f);
 }
 
-template <int DT, int C>
+template <int DT, int C, int OT>
 cudaError_t launch_forward_t(const ForwardArgs &a) {
     using S = FwdShape<DT, C>;
     FwdParams p;
@@ -562,10 +592,16 @@ cudaError_t launch_forward_t(const ForwardArgs &a) {
     if (n_compute < 1) n_compute = 1;
     p.n_compute = static_cast<int>(n_compute);
     p.n_compute_div = FastDiv(static_cast<uint32_t>(n_compute));
-    p.n_fill = static_cast<int>(div_up(a.n_cells, kFillCells));
-    p.out = static_cast<__half *>(a.out);
+    // Fill tiles: about four fill CTAs per SM (each costs a dependent search
+    // before its stores, so large grids take larger tiles).
+    int fill_cells = kFillCellsMin;
+    while (fill_cells < kFillCellsMax && a.n_cells > static_cast<int64_t>(fill_cells) * 4 * (a.sm_count > 0 ? a.sm_count : 148))
+        fill_cells *= 2;
+    p.fill_cells = fill_cells;
+    p.n_fill = static_cast<int>(div_up(a.n_cells, fill_cells));
+    p.out = static_cast<unsigned char *>(a.out);
     const int grid = p.n_compute + p.n_fill;
-    k_forward<DT, C><<<grid, kThreads, 0, a.stream>>>(p);
+    k_forward<DT, C, OT><<<grid, kThreads, 0, a.stream>>>(p);
     count_launch();
     return cudaGetLastError();
 }

@@ -204,6 +204,34 @@ BEVPOOL_API bevpool_status bevpool_forward(bevpool_dtype dtype, const void *dept
                                int32_t n_cells, void *out, void *stream);
 
 /*
+ * The forward with an FP8 output: the pages' FP8 path halves output bytes as
+ * well as feature bytes (section "Eliminate redundant scatter traffic",
+ * Figure 4; section "Map the algorithm to hardware" keeps depth and output
+ * in FP8).  Same arguments and semantics as bevpool_forward, except that
+ * every output value v (including the input scales) is stored as the OCP
+ * E4M3 code nearest to v / out_scale, computed from the FP32 sum (round to
+ * nearest even, magnitudes above 448 saturate to +-448); cells no interval
+ * names get the code 0x00.
+ *
+ *   out_scale         per-tensor output scale, finite and > 0 (e.g. from a
+ *                     calibration: max |output| / 448).
+ *   out               device, [n_cells, C] uint8 E4M3 codes, 16-byte
+ *                     aligned; fully overwritten.
+ *
+ * Requires C % 16 == 0 (rows of whole 16-byte vectors) besides
+ * bevpool_forward_supported(dtype, C); other C give BEVPOOL_ERR_UNSUPPORTED.
+ * A non-positive or non-finite out_scale gives BEVPOOL_ERR_INVALID_ARG.
+ */
+BEVPOOL_API bevpool_status bevpool_forward_e4m3_out(bevpool_dtype dtype, const void *depth, const void *feat,
+                                        int32_t NC, int32_t D, int32_t H, int32_t W, int32_t C,
+                                        float depth_scale, float feat_scale, float out_scale,
+                                        const int32_t *ranks_depth, const int32_t *ranks_feat,
+                                        const int32_t *ranks_bev, const int32_t *interval_starts,
+                                        const int32_t *interval_lengths, int32_t n_points,
+                                        int32_t n_intervals, const int32_t *d_counts, int32_t n_cells,
+                                        void *out, void *stream);
+
+/*
  * Check a scatter map on the device (debug aid; the five-array map of the
  * section "Eliminate redundant scatter traffic" with the interval structure
  * of the section "Implement interval-owned scatter-reduce").  Writes to

@@ -50,3 +50,62 @@ def assert_forward_close(wl, got, ref):
     tol = tolerance(wl, ref)
     assert err <= tol, f"{wl.name}: max abs err {err:.3g} above tolerance {tol:.3g}"
     return err
+
+
+# ---------------------------------------------------------------- E4M3 output
+
+def _abs_inputs(wl):
+    """|depth|, |feat| codes of the workload (sign bit cleared)."""
+    if wl.dtype == "f16":
+        d = np.ascontiguousarray(wl.depth).view(np.uint16) & np.uint16(0x7FFF)
+        f = np.ascontiguousarray(wl.feat).view(np.uint16) & np.uint16(0x7FFF)
+    else:
+        d = np.ascontiguousarray(wl.depth).view(np.uint8) & np.uint8(0x7F)
+        f = np.ascontiguousarray(wl.feat).view(np.uint8) & np.uint8(0x7F)
+    return d, f
+
+
+def oracle_e4m3_out(wl, out_scale):
+    """(codes, exact values v = value / out_scale, FP32 error window) for the
+    E4M3-output forward.  The window bounds |v_fp32 - v| for a GPU that sums
+    exact products in FP32 (one rounding per point, per partial-row combine
+    and for the scale): (2L + 8) * 2^-24 * sum|d f| * scale, L the longest
+    interval."""
+    import oracle
+
+    codes, v = oracle.forward_e4m3_out(wl.dtype, wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat,
+                                       wl.depth_scale, wl.feat_scale, out_scale)
+    d_abs, f_abs = _abs_inputs(wl)
+    s_abs = oracle.forward(wl.dtype, wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, d_abs, f_abs,
+                           wl.depth_scale, wl.feat_scale) / out_scale
+    kept = wl.cell_ids[wl.cell_ids >= 0]
+    L = int(np.bincount(kept).max()) if kept.size else 0
+    window = (2 * L + 8) * 2.0 ** -24 * np.abs(s_abs)
+    return codes, v, window
+
+
+def assert_e4m3_out_matches(wl, got, out_scale):
+    """Every E4M3 code equals the oracle's nearest code, except where the exact
+    value lies within the FP32 error window of the midpoint between that code
+    and the GPU's (adjacent) one."""
+    import oracle
+
+    g = got.cpu().numpy().reshape(wl.n_cells, wl.C)
+    codes, v, window = oracle_e4m3_out(wl, out_scale)
+    gv = oracle.e4m3_to_double(g)
+    wv = oracle.e4m3_to_double(codes)
+    assert not np.isnan(gv).any(), "NaN code in the output"
+    diff = gv != wv
+    if diff.any():
+        vi, gi, wi, win = v[diff], gv[diff], wv[diff], window[diff]
+        mid = (gi + wi) / 2
+        # adjacent codes: nothing representable strictly between them
+        lo, hi = np.minimum(gi, wi), np.maximum(gi, wi)
+        all_vals = np.unique(oracle.e4m3_to_double(np.arange(256, dtype=np.uint16).astype(np.uint8)))
+        all_vals = all_vals[~np.isnan(all_vals)]
+        between = np.array([np.any((all_vals > a) & (all_vals < b)) for a, b in zip(lo, hi)])
+        near_mid = np.abs(vi - mid) <= win
+        bad = between | ~near_mid
+        assert not bad.any(), (f"{wl.name}: {int(bad.sum())} codes off the nearest one "
+                               f"(first at value {vi[bad][0]!r}: got {gi[bad][0]!r}, want {wi[bad][0]!r})")
+    return int(diff.sum())

@@ -119,3 +119,16 @@ def test_validate_map_rejects_bad_arguments(bp):
                 n_points=10, n_intervals=3, NC=1, D=2, H=3, W=4, n_cells=9, d_result=FAKE, h_result=None, stream=0)
     for change in [dict(d_result=0), dict(NC=0), dict(n_points=-1), dict(ranks_bev=0), dict(interval_lengths=0)]:
         assert bp.bevpool_validate_map(**{**args, **change}) == bp.BEVPOOL_ERR_INVALID_ARG, change
+
+
+def test_forward_e4m3_out_rejects_bad_arguments(bp):
+    args = dict(dtype=bp.BEVPOOL_F16, depth=FAKE, feat=FAKE, NC=2, D=3, H=4, W=5, C=80, depth_scale=1.0,
+                feat_scale=1.0, out_scale=0.5, ranks_depth=FAKE, ranks_feat=FAKE, ranks_bev=FAKE,
+                interval_starts=FAKE, interval_lengths=FAKE, n_points=50, n_intervals=20, d_counts=None,
+                n_cells=30, out=FAKE, stream=0)
+    for change in [dict(C=72), dict(C=8), dict(dtype=3)]:
+        assert bp.bevpool_forward_e4m3_out(**{**args, **change}) == bp.BEVPOOL_ERR_UNSUPPORTED, change
+    bad = [dict(out_scale=0.0), dict(out_scale=-1.0), dict(out_scale=float("inf")), dict(out_scale=float("nan")),
+           dict(out_scale=1e-38, depth_scale=1e30), dict(out=FAKE + 4), dict(NC=0), dict(n_points=121)]
+    for change in bad:
+        assert bp.bevpool_forward_e4m3_out(**{**args, **change}) == bp.BEVPOOL_ERR_INVALID_ARG, change
