@@ -434,8 +434,9 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="canonical",
-                    choices=["tiny", "canonical", "canonical_fp8", "bevdet", "dram_batch"])
+    from depth_weighted_scatter_gb300 import workloads
+
+    ap.add_argument("--config", default="canonical", choices=workloads.ALL_NAMES)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--out-dtype", choices=["f16", "e4m3"], default="f16",
                     help="output of the forward: fp16, or E4M3 codes (bevpool_forward_e4m3_out)")

@@ -52,6 +52,13 @@
 #define BEVPOOL_FWD_LANE_BYTES 16   // bytes of a feature row each lane loads (16 or 32) for wide rows
 #endif
 
+#ifndef BEVPOOL_FWD_E4M3_LANE_BYTES
+#define BEVPOOL_FWD_E4M3_LANE_BYTES 16   // bytes of an E4M3 feature row each lane loads
+#endif
+#ifndef BEVPOOL_FWD_E4M3_BATCH16
+#define BEVPOOL_FWD_E4M3_BATCH16 5       // points in flight per owner for E4M3 rows read 16 bytes per lane (registers: 5 rows of 16 B next to 16 FP32 sums)
+#endif
+
 #ifndef BEVPOOL_FMA_VARIANT
 #define BEVPOOL_FMA_VARIANT 1   // 0: convert to f32 + FFMA, 1: f16 x f16 + f32 FMA, 2: convert + packed f32x2 FMA
 #endif
@@ -78,14 +85,15 @@ template <int DT, int C>
 struct FwdShape {
     static constexpr int EB = DT == kDtypeF16 ? 2 : 1;          // input bytes per element
     static constexpr int ROWB = C * EB;                         // bytes per feature row
-    static constexpr int VB = ROWB >= 4 * BEVPOOL_FWD_LANE_BYTES && ROWB % BEVPOOL_FWD_LANE_BYTES == 0
-                                  ? BEVPOOL_FWD_LANE_BYTES
+    static constexpr int LANE_BYTES = DT == kDtypeF16 ? BEVPOOL_FWD_LANE_BYTES : BEVPOOL_FWD_E4M3_LANE_BYTES;
+    static constexpr int VB = ROWB >= 4 * LANE_BYTES && ROWB % LANE_BYTES == 0
+                                  ? LANE_BYTES
                                   : (ROWB >= 64 ? 16 : ROWB / 4);   // bytes per lane (>= 4 lanes per owner)
     static constexpr int LPO = ROWB / VB;                       // lanes per owner
     static constexpr int EPL = VB / EB;                         // channels per lane
     static constexpr int OPW = 32 / LPO;                        // owners per warp
     static constexpr int OWNERS = kWarps * OPW;                 // owners per CTA
-    static constexpr int BATCH_CFG = VB >= 32 ? 4 : ((DT == kDtypeF16 || VB < 16) ? BEVPOOL_FWD_BATCH : 4);
+    static constexpr int BATCH_CFG = VB >= 32 ? 4 : ((DT == kDtypeF16 || VB < 16) ? BEVPOOL_FWD_BATCH : BEVPOOL_FWD_E4M3_BATCH16);
     static constexpr int BATCH = BATCH_CFG < LPO ? BATCH_CFG : LPO;   // points in flight per owner (<= LPO)
     static_assert(ROWB % VB == 0 && (VB == 2 || VB == 4 || VB == 8 || VB == 16 || VB == 32), "bad vector width");
     static_assert(LPO >= 4 && LPO <= 32, "bad lane mapping");
@@ -185,6 +193,19 @@ __device__ __forceinline__ void fma_h2(float &a0, float &a1, unsigned short d, u
 #endif
 }
 
+// acc[0..4) += d * (four E4M3 codes of w, lowest byte first): each pair of
+// codes widens to two fp16 values in one conversion (exact), then FP32 FMAs.
+__device__ __forceinline__ void fma_e4m3x4(float *acc, unsigned short d, uint32_t w) {
+    asm("{\n\t.reg .b16 lo, hi;\n\t.reg .b32 p0, p1;\n\t.reg .f16 a0, a1, a2, a3;\n\t"
+        "mov.b32 {lo, hi}, %4;\n\t"
+        "cvt.rn.f16x2.e4m3x2 p0, lo;\n\tcvt.rn.f16x2.e4m3x2 p1, hi;\n\t"
+        "mov.b32 {a0, a1}, p0;\n\tmov.b32 {a2, a3}, p1;\n\t"
+        "fma.rn.f32.f16 %0, %5, a0, %0;\n\tfma.rn.f32.f16 %1, %5, a1, %1;\n\t"
+        "fma.rn.f32.f16 %2, %5, a2, %2;\n\tfma.rn.f32.f16 %3, %5, a3, %3;\n\t}"
+        : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3])
+        : "r"(w), "h"(d));
+}
+
 // acc[0 .. EPL) += d * decode(raw)
 template <int DT, int VB>
 __device__ __forceinline__ void fma_vec(float *acc, unsigned short d, const RawVec<VB> &raw) {
@@ -205,14 +226,7 @@ __device__ __forceinline__ void fma_vec(float *acc, unsigned short d, const RawV
             fma_h2(acc[0], acc[1], d, static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16));
         } else {
 #pragma unroll
-            for (int i = 0; i < VB / 4; ++i) {
-                const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
-                    static_cast<__nv_fp8x2_storage_t>(raw.w[i] & 0xffffu), __NV_E4M3);
-                const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
-                    static_cast<__nv_fp8x2_storage_t>(raw.w[i] >> 16), __NV_E4M3);
-                fma_h2(acc[4 * i + 0], acc[4 * i + 1], d, static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16));
-                fma_h2(acc[4 * i + 2], acc[4 * i + 3], d, static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16));
-            }
+            for (int i = 0; i < VB / 4; ++i) fma_e4m3x4(acc + 4 * i, d, raw.w[i]);
         }
     }
 }

@@ -112,6 +112,22 @@ def _ring_cells(rng: np.random.Generator, n: int, centre: float, r_in: float, r_
 RING_EXPONENT = 1.6
 
 
+def _ring(name: str, seed: int, keep_p: float, C: int) -> Workload:
+    """The canonical frustum (6 cameras, D=118, 32x88 features) into the
+    360x360 ring grid, keeping each frustum point with probability keep_p."""
+    NC, D, H, W, Y, X = 6, 118, 32, 88, 360, 360
+    rng = np.random.default_rng(seed)
+    feat = _normal_feat(rng, NC, H, W, C)
+    depth = _softmax_depth(rng, NC, D, H, W, 2.0)
+    nf = NC * D * H * W
+    keep = rng.random(nf) < keep_p
+    cells = np.full(nf, -1, dtype=np.int32)
+    cells[keep] = _ring_cells(rng, int(keep.sum()), 180.0, 40.0, 110.0, RING_EXPONENT, X)
+    return Workload(name, NC, D, H, W, C, Y * X, cells, depth, feat, grid=(1, Y, X),
+                    recipe=f"seed {seed}: feat N(0,1) fp16; depth softmax over D of N(0,sigma=2) logits; "
+                           f"keep Bernoulli({keep_p}); ring r=40+110*u^{RING_EXPONENT}, theta~U(0,2pi)")
+
+
 def canonical(seed: int = 1) -> Workload:
     """6 cameras, D=118, 32x88 features, C=80, 360x360 grid (1,993,728 frustum points).
 
@@ -119,35 +135,48 @@ def canonical(seed: int = 1) -> Workload:
     lands in a ring of radius 40..150 cells around the grid centre with
     r = 40 + 110*u**1.6, so cells near the inner edge collect more points and
     interval lengths are skewed (1 up to about 60)."""
-    NC, D, H, W, C, Y, X = 6, 118, 32, 88, 80, 360, 360
-    rng = np.random.default_rng(seed)
-    feat = _normal_feat(rng, NC, H, W, C)
-    depth = _softmax_depth(rng, NC, D, H, W, 2.0)
-    nf = NC * D * H * W
-    keep = rng.random(nf) < 0.105
-    cells = np.full(nf, -1, dtype=np.int32)
-    cells[keep] = _ring_cells(rng, int(keep.sum()), 180.0, 40.0, 110.0, RING_EXPONENT, X)
-    return Workload("canonical", NC, D, H, W, C, Y * X, cells, depth, feat, grid=(1, Y, X),
-                    recipe=f"seed {seed}: feat N(0,1) fp16; depth softmax over D of N(0,sigma=2) logits; "
-                           f"keep Bernoulli(0.105); ring r=40+110*u^{RING_EXPONENT}, theta~U(0,2pi)")
+    return _ring("canonical", seed, 0.105, 80)
 
 
-def canonical_fp8(seed: int = 1) -> Workload:
-    """The canonical workload (same cell ids) with feat and depth as E4M3.
-
-    feat_scale = max|feat| / 448 and depth_scale = max(depth), so the depth
-    codes lie in [0, 1]; codes are round-to-nearest-even of value/scale."""
-    wl = canonical(seed)
+def _to_fp8(wl: Workload, name: str) -> Workload:
+    """The same workload with feat and depth as E4M3: feat_scale =
+    max|feat| / 448 and depth_scale = max(depth), so the depth codes lie in
+    [0, 1]; codes are round-to-nearest-even of value/scale."""
     f32 = wl.feat.astype(np.float32)
     d32 = wl.depth.astype(np.float32)
     fs = float(np.float32(np.abs(f32).max() / np.float32(E4M3_MAX)))
     ds = float(np.float32(d32.max()))
     return dataclasses.replace(
-        wl, name="canonical_fp8", dtype="e4m3",
+        wl, name=name, dtype="e4m3",
         feat=quantize_e4m3(f32, fs).reshape(wl.feat.shape),
         depth=quantize_e4m3(d32, ds).reshape(wl.depth.shape),
         feat_scale=fs, depth_scale=ds,
         recipe=wl.recipe + "; then E4M3 with feat_scale=max|feat|/448, depth_scale=max(depth)")
+
+
+def canonical_fp8(seed: int = 1) -> Workload:
+    """The canonical workload (same cell ids) with feat and depth as E4M3."""
+    return _to_fp8(canonical(seed), "canonical_fp8")
+
+
+# The shapes of the pages' Table 1 ("Map the algorithm to hardware"): only C
+# is printed, so the point counts are synthetic.  The V2 column's latencies
+# (137.8 / 274.0 / 749.9 / 1,675.0 us for small / canonical / large / very
+# large) grow with the number of scattered points, so the keep probabilities
+# scale the canonical 0.105 by 0.50, 2.74 and 6.11; the wide configs keep the
+# canonical points with C = 128 and 256.
+TABLE1 = {
+    "table1_small": (21, 0.105 * 137.8 / 274.0, 80),
+    "table1_large": (22, 0.105 * 749.9 / 274.0, 80),
+    "table1_very_large": (23, 0.105 * 1675.0 / 274.0, 80),
+    "wide_c128": (24, 0.105, 128),
+    "wide_c256": (25, 0.105, 256),
+}
+
+
+def table1(name: str) -> Workload:
+    seed, keep_p, C = TABLE1[name]
+    return _ring(name, seed, round(keep_p, 4), C)
 
 
 def bevdet(seed: int = 3) -> Workload:
@@ -253,4 +282,14 @@ CONFIGS = {
 
 
 def make(name: str) -> Workload:
-    return CONFIGS[name]()
+    """A named workload; '<table-1 shape>_fp8' gives its E4M3 version."""
+    if name in CONFIGS:
+        return CONFIGS[name]()
+    if name in TABLE1:
+        return table1(name)
+    if name.endswith("_fp8") and name[:-4] in TABLE1:
+        return _to_fp8(table1(name[:-4]), name)
+    raise KeyError(f"unknown workload {name!r}")
+
+
+ALL_NAMES = list(CONFIGS) + list(TABLE1) + [n + "_fp8" for n in TABLE1]
