@@ -61,6 +61,9 @@ _lib.bevpool_forward.restype = ctypes.c_int
 _lib.bevpool_forward_e4m3_out.argtypes = [ctypes.c_int, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _f32,
                                           _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp]
 _lib.bevpool_forward_e4m3_out.restype = ctypes.c_int
+_lib.bevpool_pool_frame.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _vp, _vp, _i32, _f32, _f32,
+                                    _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]
+_lib.bevpool_pool_frame.restype = ctypes.c_int
 _lib.bevpool_validate_map.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]
 _lib.bevpool_validate_map.restype = ctypes.c_int
 
@@ -131,6 +134,15 @@ def bevpool_forward_e4m3_out(dtype: int, depth: int, feat: int, NC: int, D: int,
     return _lib.bevpool_forward_e4m3_out(dtype, depth, feat, NC, D, H, W, C, depth_scale, feat_scale, out_scale,
                                          ranks_depth, ranks_feat, ranks_bev, interval_starts, interval_lengths,
                                          n_points, n_intervals, d_counts, n_cells, out, stream)
+
+
+def bevpool_pool_frame(cell_ids: int, NC: int, D: int, H: int, W: int, n_cells: int, dtype: int, depth: int,
+                       feat: int, C: int, depth_scale: float, feat_scale: float, ranks_depth: int, ranks_feat: int,
+                       ranks_bev: int, interval_starts: int, interval_lengths: int, d_counts: int, workspace: int,
+                       workspace_bytes: int, out: int, stream: int) -> int:
+    return _lib.bevpool_pool_frame(cell_ids, NC, D, H, W, n_cells, dtype, depth, feat, C, depth_scale, feat_scale,
+                                   ranks_depth, ranks_feat, ranks_bev, interval_starts, interval_lengths, d_counts,
+                                   workspace, workspace_bytes, out, stream)
 
 
 def bevpool_validate_map(ranks_depth: int, ranks_feat: int, ranks_bev: int, interval_starts: int,
@@ -268,3 +280,24 @@ def validate_map(m: ScatterMap, stream=None) -> int:
     if st not in (BEVPOOL_OK, BEVPOOL_ERR_OUT_OF_RANGE):
         raise BevpoolError(st, "bevpool_validate_map")
     return int(h[0])
+
+
+def pool_frame(cell_ids, depth, feat, NC: int, D: int, H: int, W: int, n_cells: int, C: int, *,
+               dtype: int = BEVPOOL_F16, depth_scale: float = 1.0, feat_scale: float = 1.0,
+               out=None, map_out: Optional[ScatterMap] = None, workspace=None, stream=None):
+    """bevpool_pool_frame: the map build and the forward of one frame, no host sync.
+    Returns (out, map); the map's host counts stay unknown (read d_counts)."""
+    import torch
+
+    m = map_out if map_out is not None else ScatterMap.allocate(NC, D, H, W, n_cells, cell_ids.device)
+    ws = workspace if workspace is not None else workspace_for(NC, D, H, W, n_cells, cell_ids.device)
+    if out is None:
+        out = torch.empty((n_cells, C), dtype=torch.float16, device=feat.device)
+    st = bevpool_pool_frame(cell_ids.data_ptr(), NC, D, H, W, n_cells, dtype, depth.data_ptr(), feat.data_ptr(), C,
+                            depth_scale, feat_scale, m.ranks_depth.data_ptr(), m.ranks_feat.data_ptr(),
+                            m.ranks_bev.data_ptr(), m.interval_starts.data_ptr(), m.interval_lengths.data_ptr(),
+                            m.d_counts.data_ptr(), ws.data_ptr(), ws.numel(), out.data_ptr(), _stream(stream))
+    if st != BEVPOOL_OK:
+        raise BevpoolError(st, "bevpool_pool_frame")
+    m.n_points = m.n_intervals = None
+    return out, m

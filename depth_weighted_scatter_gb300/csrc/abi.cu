@@ -290,6 +290,32 @@ bevpool_status bevpool_forward_e4m3_out(bevpool_dtype dtype, const void *depth, 
                         n_cells, out, stream);
 }
 
+bevpool_status bevpool_pool_frame(const int32_t *cell_ids, int32_t NC, int32_t D, int32_t H, int32_t W,
+                                  int32_t n_cells, bevpool_dtype dtype, const void *depth, const void *feat,
+                                  int32_t C, float depth_scale, float feat_scale, int32_t *ranks_depth,
+                                  int32_t *ranks_feat, int32_t *ranks_bev, int32_t *interval_starts,
+                                  int32_t *interval_lengths, int32_t *d_counts, void *workspace,
+                                  size_t workspace_bytes, void *out, void *stream) {
+    // Everything the two calls would reject is checked before either enqueues work.
+    if (dtype != BEVPOOL_F16 && dtype != BEVPOOL_E4M3) return BEVPOOL_ERR_UNSUPPORTED;
+    if (!forward_supported(static_cast<int>(dtype), C)) return BEVPOOL_ERR_UNSUPPORTED;
+    if (!frustum_ok(NC, D, H, W) || n_cells < 1) return BEVPOOL_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(n_cells) * C > INT32_MAX) return BEVPOOL_ERR_INVALID_ARG;
+    if (!depth || !feat || !out || !aligned(feat, 16) || !aligned(out, 16)) return BEVPOOL_ERR_INVALID_ARG;
+    if (dtype == BEVPOOL_F16 && !aligned(depth, 2)) return BEVPOOL_ERR_INVALID_ARG;
+    if (!std::isfinite(depth_scale * feat_scale)) return BEVPOOL_ERR_INVALID_ARG;
+    bevpool_status st = bevpool_build_map(cell_ids, NC, D, H, W, n_cells, ranks_depth, ranks_feat, ranks_bev,
+                                          interval_starts, interval_lengths, d_counts, nullptr, workspace,
+                                          workspace_bytes, stream);
+    if (st != BEVPOOL_OK) return st;
+    const int64_t nf = static_cast<int64_t>(NC) * D * H * W;
+    const int32_t cap_points = static_cast<int32_t>(nf);
+    const int32_t cap_intervals = static_cast<int32_t>(nf < n_cells ? nf : n_cells);
+    return bevpool_forward(dtype, depth, feat, NC, D, H, W, C, depth_scale, feat_scale, ranks_depth, ranks_feat,
+                           ranks_bev, interval_starts, interval_lengths, cap_points, cap_intervals, d_counts,
+                           n_cells, out, stream);
+}
+
 bevpool_status bevpool_validate_map(const int32_t *ranks_depth, const int32_t *ranks_feat, const int32_t *ranks_bev,
                                     const int32_t *interval_starts, const int32_t *interval_lengths,
                                     int32_t n_points, int32_t n_intervals, int32_t NC, int32_t D, int32_t H,

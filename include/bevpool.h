@@ -232,6 +232,30 @@ BEVPOOL_API bevpool_status bevpool_forward_e4m3_out(bevpool_dtype dtype, const v
                                         void *out, void *stream);
 
 /*
+ * One frame with its own geometry: bevpool_build_map (no host
+ * synchronisation) followed on the same stream by bevpool_forward reading
+ * the counts on the device, for pipelines whose cell ids change every frame
+ * (the pages prepare the map ahead, section "Implement interval-owned
+ * scatter-reduce"; this puts the build next to the forward in one call).
+ * Nothing is copied to the host, so the call can be captured in a CUDA graph
+ * and replayed with new cell_ids / depth / feat in the same buffers.
+ *
+ * Arguments are those of bevpool_build_map (the five map arrays with
+ * capacity NC*D*H*W, d_counts, the workspace) and of bevpool_forward
+ * (dtype, depth, feat, C, the scales, out [n_cells, C] fp16).  The map is
+ * left in the arrays for later use; d_counts[2] counts invalid cell ids
+ * (treated as dropped).  The result is bit-identical to the two calls made
+ * one after the other with the same capacities (NC*D*H*W points and
+ * min(NC*D*H*W, n_cells) intervals).
+ */
+BEVPOOL_API bevpool_status bevpool_pool_frame(const int32_t *cell_ids, int32_t NC, int32_t D, int32_t H,
+                                  int32_t W, int32_t n_cells, bevpool_dtype dtype, const void *depth,
+                                  const void *feat, int32_t C, float depth_scale, float feat_scale,
+                                  int32_t *ranks_depth, int32_t *ranks_feat, int32_t *ranks_bev,
+                                  int32_t *interval_starts, int32_t *interval_lengths, int32_t *d_counts,
+                                  void *workspace, size_t workspace_bytes, void *out, void *stream);
+
+/*
  * Check a scatter map on the device (debug aid; the five-array map of the
  * section "Eliminate redundant scatter traffic" with the interval structure
  * of the section "Implement interval-owned scatter-reduce").  Writes to

@@ -132,3 +132,17 @@ def test_forward_e4m3_out_rejects_bad_arguments(bp):
            dict(out_scale=1e-38, depth_scale=1e30), dict(out=FAKE + 4), dict(NC=0), dict(n_points=121)]
     for change in bad:
         assert bp.bevpool_forward_e4m3_out(**{**args, **change}) == bp.BEVPOOL_ERR_INVALID_ARG, change
+
+
+def test_pool_frame_rejects_bad_arguments(bp):
+    nf = 2 * 3 * 4 * 5
+    ws = bp.bevpool_build_map_workspace_size(nf, 30)
+    args = dict(cell_ids=FAKE, NC=2, D=3, H=4, W=5, n_cells=30, dtype=bp.BEVPOOL_F16, depth=FAKE, feat=FAKE, C=80,
+                depth_scale=1.0, feat_scale=1.0, ranks_depth=FAKE, ranks_feat=FAKE, ranks_bev=FAKE,
+                interval_starts=FAKE, interval_lengths=FAKE, d_counts=FAKE, workspace=FAKE, workspace_bytes=ws,
+                out=FAKE, stream=0)
+    assert bp.bevpool_pool_frame(**{**args, "C": 72}) == bp.BEVPOOL_ERR_UNSUPPORTED
+    for change in [dict(NC=0), dict(n_cells=0), dict(feat=FAKE + 8), dict(out=0), dict(cell_ids=0),
+                   dict(depth_scale=float("inf"))]:
+        assert bp.bevpool_pool_frame(**{**args, **change}) == bp.BEVPOOL_ERR_INVALID_ARG, change
+    assert bp.bevpool_pool_frame(**{**args, "workspace_bytes": ws - 1}) == bp.BEVPOOL_ERR_WORKSPACE
