@@ -39,12 +39,13 @@ class Workload:
     n_cells: int
     cell_ids: np.ndarray          # int32 [NC*D*H*W]
     depth: np.ndarray             # float16 [NC,D,H,W]  or uint8 E4M3 codes
-    feat: np.ndarray              # float16 [NC,H,W,C]  or uint8 E4M3 codes
-    dtype: str = "f16"            # "f16" or "e4m3"
-    depth_scale: float = 1.0      # E4M3 only: depth value = code * depth_scale
-    feat_scale: float = 1.0       # E4M3 only: feat value = code * feat_scale
+    feat: np.ndarray              # float16 [NC,H,W,C], uint8 E4M3 codes, or uint8 [NC,H,W,C/2] E2M1 pairs
+    dtype: str = "f16"            # "f16", "e4m3" or "nvfp4" (E2M1 features, E4M3 depth)
+    depth_scale: float = 1.0      # E4M3 depth: depth value = code * depth_scale
+    feat_scale: float = 1.0       # E4M3 / NVFP4 feat: per-tensor factor of every feature value
     grid: tuple = ()              # (B, Y, X) of the BEV grid, n_cells = B*Y*X
     recipe: str = ""
+    feat_block: Optional[np.ndarray] = None   # NVFP4: uint8 [NC,H,W,C/16] E4M3 scale of each 16-element block
 
     @property
     def n_frustum(self) -> int:
@@ -80,6 +81,44 @@ def quantize_e4m3(x: np.ndarray, scale: float) -> np.ndarray:
     t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)) / torch.tensor(scale, dtype=torch.float32)
     q = t.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
     return q.view(torch.uint8).numpy().copy()
+
+
+E2M1_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])   # magnitudes of the codes 0..7
+
+
+def quantize_e2m1(x: np.ndarray) -> np.ndarray:
+    """E2M1 codes (0..15) of x: the nearest magnitude, ties to the even
+    code, saturating at 6; bit 3 is the sign."""
+    a = np.minimum(np.abs(x), 6.0)
+    dist = np.abs(a[..., None] - E2M1_VALUES)
+    best = dist.min(axis=-1, keepdims=True)
+    tie_ok = (dist == best) & ((np.arange(8) & 1) == 0)
+    plain = dist == best
+    pick = np.where(tie_ok.any(axis=-1), np.argmax(tie_ok, axis=-1), np.argmax(plain, axis=-1))
+    code = pick.astype(np.uint8)
+    return np.where(np.signbit(x) & (code != 0), code | 8, code).astype(np.uint8)
+
+
+def quantize_nvfp4(feat: np.ndarray):
+    """Two-level NVFP4 quantisation of an [..., C] fp32 tensor (C % 16 == 0):
+    feat_scale = max|feat| / (6 * 448) per tensor, one E4M3 block scale per 16
+    elements (block max / 6 / feat_scale, rounded to nearest even), E2M1
+    elements of value / (block scale * feat_scale).  Returns (packed nibbles
+    [..., C/2] with element 2i in the low nibble of byte i, block scales
+    [..., C/16], feat_scale)."""
+    f = np.ascontiguousarray(feat, dtype=np.float32)
+    C = f.shape[-1]
+    fs = float(np.float32(max(float(np.abs(f).max()), 1e-30) / (6.0 * E4M3_MAX)))
+    blocks = f.reshape(f.shape[:-1] + (C // 16, 16))
+    bmax = np.abs(blocks).max(axis=-1)
+    bcode = quantize_e4m3(bmax / 6.0, fs)
+    import torch
+
+    bval = torch.from_numpy(bcode).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    denom = np.where(bval > 0, bval * fs, 1.0)
+    q = quantize_e2m1(np.where(bval[..., None] > 0, blocks / denom[..., None], 0.0)).reshape(f.shape)
+    packed = (q[..., 0::2] | (q[..., 1::2] << 4)).astype(np.uint8)
+    return packed, bcode, fs
 
 
 def tiny(seed: int = 0) -> Workload:
@@ -152,6 +191,19 @@ def _to_fp8(wl: Workload, name: str) -> Workload:
         depth=quantize_e4m3(d32, ds).reshape(wl.depth.shape),
         feat_scale=fs, depth_scale=ds,
         recipe=wl.recipe + "; then E4M3 with feat_scale=max|feat|/448, depth_scale=max(depth)")
+
+
+def _to_nvfp4(wl: Workload, name: str) -> Workload:
+    """The same workload with NVFP4 features (quantize_nvfp4) and E4M3 depth
+    (depth_scale = max(depth), as in the FP8 workloads)."""
+    d32 = wl.depth.astype(np.float32)
+    ds = float(np.float32(d32.max()))
+    packed, blocks, fs = quantize_nvfp4(wl.feat.astype(np.float32))
+    return dataclasses.replace(
+        wl, name=name, dtype="nvfp4", feat=packed, feat_block=blocks, feat_scale=fs,
+        depth=quantize_e4m3(d32, ds).reshape(wl.depth.shape), depth_scale=ds,
+        recipe=wl.recipe + "; then NVFP4 features (E2M1, E4M3 scale per 16, feat_scale=max|feat|/2688) "
+                           "and E4M3 depth (depth_scale=max(depth))")
 
 
 def canonical_fp8(seed: int = 1) -> Workload:
@@ -289,7 +341,12 @@ def make(name: str) -> Workload:
         return table1(name)
     if name.endswith("_fp8") and name[:-4] in TABLE1:
         return _to_fp8(table1(name[:-4]), name)
+    if name == "canonical_nvfp4":
+        return _to_nvfp4(canonical(), name)
+    if name.endswith("_nvfp4") and name[:-6] in TABLE1:
+        return _to_nvfp4(table1(name[:-6]), name)
     raise KeyError(f"unknown workload {name!r}")
 
 
-ALL_NAMES = list(CONFIGS) + list(TABLE1) + [n + "_fp8" for n in TABLE1]
+ALL_NAMES = (list(CONFIGS) + ["canonical_nvfp4"] + list(TABLE1) + [n + "_fp8" for n in TABLE1] +
+             [n + "_nvfp4" for n in TABLE1])

@@ -64,6 +64,8 @@ def _load():
             lib.oracle_half_array_to_double.restype = None
             lib.oracle_e4m3_array_to_double.argtypes = [vp, i64, vp]
             lib.oracle_double_array_to_e4m3.argtypes = [vp, i64, vp]
+            lib.oracle_e2m1_array_to_double.argtypes = [vp, i64, vp]
+            lib.oracle_forward_nvfp4.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, dbl, dbl, vp]
             lib.oracle_e4m3_array_to_double.restype = None
             lib.oracle_build_map.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
             lib.oracle_build_map.restype = ctypes.c_int
@@ -90,6 +92,37 @@ def e4m3_to_double(codes: np.ndarray) -> np.ndarray:
     src = np.ascontiguousarray(codes).view(np.uint8)
     out = np.empty(src.shape, dtype=np.float64)
     _load().oracle_e4m3_array_to_double(_ptr(src), src.size, _ptr(out))
+    return out
+
+
+def e2m1_to_double(nibbles: np.ndarray) -> np.ndarray:
+    """Values of OCP E2M1 codes (the low four bits of each entry)."""
+    c = np.ascontiguousarray(nibbles, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_e2m1_array_to_double(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def forward_nvfp4(cell_ids: np.ndarray, NC: int, D: int, H: int, W: int, n_cells: int, C: int,
+                  depth: np.ndarray, feat_packed: np.ndarray, feat_block_scales: np.ndarray,
+                  depth_scale: float, feat_scale: float) -> np.ndarray:
+    """FP64 forward with NVFP4 features: E2M1 nibbles (element 2i in the low
+    nibble of byte i of a row of C/2 bytes), one E4M3 scale per 16 elements,
+    a per-tensor feat_scale; E4M3 depth times depth_scale."""
+    cell_ids = np.ascontiguousarray(cell_ids, dtype=np.int32).reshape(-1)
+    nf = NC * D * H * W
+    if cell_ids.size != nf or C % 16 != 0:
+        raise OracleError("bad shapes for the NVFP4 forward")
+    depth = np.ascontiguousarray(depth).view(np.uint8).reshape(-1)
+    fp = np.ascontiguousarray(feat_packed).view(np.uint8).reshape(-1)
+    fb = np.ascontiguousarray(feat_block_scales).view(np.uint8).reshape(-1)
+    if depth.size != nf or fp.size != NC * H * W * C // 2 or fb.size != NC * H * W * C // 16:
+        raise OracleError("bad array sizes for the NVFP4 forward")
+    out = np.empty((n_cells, C), dtype=np.float64)
+    rc = _load().oracle_forward_nvfp4(_ptr(cell_ids), NC, D, H, W, n_cells, C, _ptr(depth), _ptr(fp), _ptr(fb),
+                                      float(depth_scale), float(feat_scale), _ptr(out))
+    if rc != OK:
+        raise OracleError(f"oracle_forward_nvfp4 failed with code {rc}")
     return out
 
 

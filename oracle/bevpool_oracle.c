@@ -35,7 +35,11 @@
  *     4: the FP8 path halves output bytes too; section "Map the algorithm to
  *     hardware": the NVFP4 experiment keeps depth and output in FP8) is the
  *     E4M3 code nearest to value / out_scale, out_scale being one per-tensor
- *     scale the caller chooses; ties to even, saturated at +-448.
+ *     scale the caller chooses; ties to even, saturated at +-448;
+ *   - NVFP4 features (section "Map the algorithm to hardware", the NVFP4
+ *     experiment: E2M1 elements with an E4M3 scale per 16 elements, depth
+ *     kept in FP8): element 2i of a row in the low nibble of byte i, the
+ *     block scales in their own [rows, C/16] array, one per-tensor factor.
  *
  * The forward oracle does NOT go through the scatter map: it walks the
  * frustum points in their original order, so it also checks the map.
@@ -86,6 +90,18 @@ double oracle_e4m3_to_double(uint8_t b)
     return sign ? -v : v;
 }
 
+/* OCP 4-bit floating point E2M1 (the element type of NVFP4): 1 sign bit,
+ * 2 exponent bits (bias 1), 1 mantissa bit, no infinities or NaN.  Exponent
+ * 0 encodes zero / the subnormal 0.5 (mantissa * 0.5). */
+double oracle_e2m1_to_double(uint8_t nibble)
+{
+    int sign = (nibble >> 3) & 1;
+    int expo = (nibble >> 1) & 3;
+    int mant = nibble & 1;
+    double v = expo == 0 ? 0.5 * mant : ldexp(1.0 + 0.5 * mant, expo - 1);
+    return sign ? -v : v;
+}
+
 /* Bulk helpers so the Python side can decode whole tensors. */
 void oracle_half_array_to_double(const uint16_t *src, int64_t n, double *dst)
 {
@@ -97,6 +113,12 @@ void oracle_e4m3_array_to_double(const uint8_t *src, int64_t n, double *dst)
 {
     for (int64_t i = 0; i < n; ++i)
         dst[i] = oracle_e4m3_to_double(src[i]);
+}
+
+void oracle_e2m1_array_to_double(const uint8_t *src, int64_t n, double *dst)
+{
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = oracle_e2m1_to_double(src[i] & 0xf);
 }
 
 /* Nearest OCP E4M3 code to x: round half to even, magnitudes above the
@@ -277,6 +299,45 @@ int oracle_forward(int32_t dtype, const int32_t *cell_ids, int32_t NC, int32_t D
                 f = oracle_half_to_double(feat16[row * C + c]);
             else
                 f = oracle_e4m3_to_double(feat8[row * C + c]) * feat_scale;
+            dst[c] += d * f;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * The forward with NVFP4 features (section "Map the algorithm to hardware",
+ * the NVFP4 experiment): feat element c of row r is the E2M1 value in nibble
+ * c of the packed row (element 2i in the low nibble of byte i), times the
+ * E4M3 block scale feat_block[r * C/16 + c/16], times the per-tensor
+ * feat_scale; depth is E4M3 times depth_scale.  Same point loop as
+ * oracle_forward, in double.
+ */
+int oracle_forward_nvfp4(const int32_t *cell_ids, int32_t NC, int32_t D, int32_t H, int32_t W,
+                         int32_t n_cells, int32_t C, const uint8_t *depth8, const uint8_t *feat4,
+                         const uint8_t *feat_block, double depth_scale, double feat_scale, double *out)
+{
+    if (NC <= 0 || D <= 0 || H <= 0 || W <= 0 || n_cells <= 0 || C <= 0 || C % 16 != 0)
+        return ORACLE_ERR_ARG;
+    int64_t n_frustum = (int64_t)NC * D * H * W;
+    memset(out, 0, (size_t)n_cells * (size_t)C * sizeof(double));
+    for (int64_t p = 0; p < n_frustum; ++p) {
+        int32_t cell = cell_ids[p];
+        if (cell == -1)
+            continue;
+        if (cell < 0 || cell >= n_cells)
+            return ORACLE_ERR_RANGE;
+        int64_t w = p % W;
+        int64_t h = (p / W) % H;
+        int64_t nc = p / ((int64_t)D * H * W);
+        int64_t row = (nc * H + h) * W + w;
+        double d = oracle_e4m3_to_double(depth8[p]) * depth_scale;
+        double *dst = out + (int64_t)cell * C;
+        for (int32_t c = 0; c < C; ++c) {
+            uint8_t byte = feat4[row * (C / 2) + c / 2];
+            uint8_t nib = (c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xf);
+            double f = oracle_e2m1_to_double(nib) * oracle_e4m3_to_double(feat_block[row * (C / 16) + c / 16]) *
+                       feat_scale;
             dst[c] += d * f;
         }
     }

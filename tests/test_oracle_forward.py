@@ -214,3 +214,79 @@ def test_e4m3_output_rejects_bad_scale():
     with pytest.raises(oracle.OracleError):
         oracle.forward_e4m3_out(wl.dtype, wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat,
                                 1.0, 1.0, 0.0)
+
+
+# ---------------------------------------------------------------- NVFP4 features
+
+def _nvfp4_decoded_feat(wl, swap_nibbles=False, block_shift=0):
+    """Feature values of an NVFP4 workload decoded independently of the
+    oracle: the E2M1 magnitudes table of the OCP format and the library's
+    E4M3 decode of the block scales."""
+    torch = pytest.importorskip("torch")
+    packed = wl.feat.reshape(wl.n_feat_rows, wl.C // 2)
+    lo, hi = packed & 0xF, packed >> 4
+    if swap_nibbles:
+        lo, hi = hi, lo
+    codes = np.empty((wl.n_feat_rows, wl.C), dtype=np.uint8)
+    codes[:, 0::2], codes[:, 1::2] = lo, hi
+    val = workloads.E2M1_VALUES[codes & 7] * np.where(codes & 8, -1.0, 1.0)
+    blocks = torch.from_numpy(wl.feat_block.reshape(wl.n_feat_rows, wl.C // 16).copy()).view(
+        torch.float8_e4m3fn).to(torch.float64).numpy()
+    blocks = np.roll(blocks, block_shift, axis=1)
+    return val * np.repeat(blocks, 16, axis=1) * wl.feat_scale
+
+
+def _nvfp4_dense(wl, F):
+    torch = pytest.importorskip("torch")
+    d = torch.from_numpy(wl.depth.reshape(-1).copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    d = d * wl.depth_scale
+    kept = wl.cell_ids >= 0
+    S = np.zeros((wl.n_cells, wl.n_frustum))
+    S[wl.cell_ids[kept], np.nonzero(kept)[0]] = 1.0
+    return S @ (d[:, None] * F[_rows(wl)])
+
+
+def _nvfp4_run(wl):
+    return oracle.forward_nvfp4(wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat, wl.feat_block,
+                                wl.depth_scale, wl.feat_scale)
+
+
+def _small_nvfp4(C=32, seed=12):
+    NC, D, H, W, cells = 2, 3, 4, 5, 30
+    rng = np.random.default_rng(seed)
+    cid = rng.integers(-1, cells, size=NC * D * H * W).astype(np.int32)
+    return workloads._to_nvfp4(workloads.custom(NC, D, H, W, C, cells, cid, seed=seed), "small_nvfp4")
+
+
+def test_e2m1_decode_matches_format_table():
+    got = oracle.e2m1_to_double(np.arange(16, dtype=np.uint8))
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]          # OCP MX E2M1 value set
+    assert np.array_equal(got[:8], mags) and np.array_equal(got[8:], [-m for m in mags])
+
+
+def test_nvfp4_forward_is_dense_product():
+    wl = _small_nvfp4()
+    out = _nvfp4_run(wl)
+    ref = _nvfp4_dense(wl, _nvfp4_decoded_feat(wl))
+    assert np.abs(out - ref).max() <= 1e-12 * max(np.abs(ref).max(), 1e-300)
+
+
+def test_nvfp4_pins_catch_planted_mistakes():
+    """Swapped nibble order or a shifted block-scale index in the decoding
+    that the oracle is compared with must be detected."""
+    wl = _small_nvfp4()
+    out = _nvfp4_run(wl)
+    for F in (_nvfp4_decoded_feat(wl, swap_nibbles=True), _nvfp4_decoded_feat(wl, block_shift=1)):
+        ref = _nvfp4_dense(wl, F)
+        assert np.abs(out - ref).max() > 1e-6 * np.abs(ref).max()
+
+
+def test_nvfp4_quantisation_round_trip_is_close():
+    """The generator's two-level quantisation keeps every value within one
+    E2M1 step of its block (a pin on the inputs, not on the oracle)."""
+    wl = workloads.make("canonical_nvfp4")
+    base = workloads.canonical()
+    F = _nvfp4_decoded_feat(wl)
+    f = base.feat.astype(np.float64).reshape(wl.n_feat_rows, wl.C)
+    blocks = np.abs(f).reshape(wl.n_feat_rows, wl.C // 16, 16).max(axis=2)
+    assert np.all(np.abs(F - f) <= np.repeat(blocks, 16, axis=1) * 0.26 + 1e-3)
