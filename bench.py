@@ -41,7 +41,7 @@ METRIC = "BEV-pool forward µs/call and GB/s vs L2/HBM roofline (209K pts, C=80,
 FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 FORWARD_SOURCES = ["forward_impl.cuh", "forward_f16.cu", "forward_e4m3.cu", "forward_f16_e4m3out.cu",
-                   "forward_e4m3_e4m3out.cu", "bevpool_internal.cuh"]
+                   "forward_e4m3_e4m3out.cu", "forward_nvfp4.cu", "forward_nvfp4_e4m3out.cu", "bevpool_internal.cuh"]
 
 
 def forward_source_hash() -> str:
@@ -82,13 +82,14 @@ def bytes_model(wl, n_points: int, n_intervals: int, out_bytes: int = 2) -> dict
     touches, once (the compulsory HBM traffic after an L2 flush);
     'gather' = what the owners actually read per point (L2-level)."""
     eb = 2 if wl.dtype == "f16" else 1
+    row = wl.C // 2 + wl.C // 16 if wl.dtype == "nvfp4" else wl.C * eb   # NVFP4: E2M1 pairs + block scales
     idx = 12 * n_points                  # ranks_depth, ranks_feat, ranks_bev
     iv = 8 * n_intervals                 # interval_starts, interval_lengths
     depth = wl.n_frustum * eb
-    feat = wl.n_feat_rows * wl.C * eb
+    feat = wl.n_feat_rows * row
     out = wl.n_cells * wl.C * out_bytes
     footprint = idx + iv + depth + feat + out
-    gather = idx + iv + n_points * eb + n_points * wl.C * eb + out
+    gather = idx + iv + n_points * eb + n_points * row + out
     return dict(index=idx, intervals=iv, depth=depth, feat=feat, out=out, footprint=footprint, gather=gather)
 
 
@@ -189,6 +190,12 @@ def oracle_call(wl, out_scale=None):
     """One oracle forward of the workload (with the E4M3 output when out_scale is given)."""
     import oracle
 
+    if wl.dtype == "nvfp4":
+        fwd = lambda: oracle.forward_nvfp4(wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat,
+                                           wl.feat_block, wl.depth_scale, wl.feat_scale)
+        if out_scale is None:
+            return fwd
+        return lambda: oracle.e4m3_from_double(fwd() / out_scale)
     if out_scale is None:
         return lambda: oracle.forward(wl.dtype, wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat,
                                       wl.depth_scale, wl.feat_scale)
@@ -226,8 +233,7 @@ def run_reference(args) -> None:
     m = oracle.build_map(wl.cell_ids, *wl.dims(), wl.n_cells)
     out_scale = None
     if args.out_dtype == "e4m3":                        # the same calibration as the GPU arm: max|output| / 448
-        ref = oracle.forward(wl.dtype, wl.cell_ids, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat,
-                             wl.depth_scale, wl.feat_scale)
+        ref = oracle_call(wl)()
         out_scale = float(np.abs(ref).max()) / 448.0 or 1.0
     call = oracle_call(wl, out_scale)
     for _ in range(args.warmup):
@@ -262,13 +268,16 @@ def run_ours(args) -> None:
     from depth_weighted_scatter_gb300 import bevpool, workloads
 
     wl = workloads.make(args.config)
-    dt = bevpool.BEVPOOL_F16 if wl.dtype == "f16" else bevpool.BEVPOOL_E4M3
+    dt = {"f16": bevpool.BEVPOOL_F16, "e4m3": bevpool.BEVPOOL_E4M3, "nvfp4": bevpool.BEVPOOL_NVFP4}[wl.dtype]
     view = np.uint16 if dt == bevpool.BEVPOOL_F16 else np.uint8
     depth_h = torch.from_numpy(np.ascontiguousarray(wl.depth).reshape(-1).view(view).copy()).pin_memory()
     feat_h = torch.from_numpy(np.ascontiguousarray(wl.feat).reshape(-1).view(view).copy()).pin_memory()
+    block_h = (torch.from_numpy(np.ascontiguousarray(wl.feat_block).reshape(-1).copy()).pin_memory()
+               if wl.feat_block is not None else None)
     cells = torch.from_numpy(wl.cell_ids).to(device)
     depth = depth_h.to(device)
     feat = feat_h.to(device)
+    block = block_h.to(device) if block_h is not None else None
 
     ws = bevpool.workspace_for(*wl.dims(), wl.n_cells, device)
     m = bevpool.ScatterMap.allocate(*wl.dims(), wl.n_cells, device)
@@ -279,7 +288,7 @@ def run_ours(args) -> None:
     out_scale = None
     if e4m3_out:                                        # calibration (untimed): max|output| / 448
         probe = bevpool.forward(m, depth, feat, wl.C, dtype=dt, depth_scale=wl.depth_scale,
-                                feat_scale=wl.feat_scale, capacity=cap)
+                                feat_scale=wl.feat_scale, capacity=cap, feat_block=block)
         out_scale = float(probe.float().abs().max().item()) / 448.0 or 1.0
         del probe
     out = torch.empty((wl.n_cells, wl.C), dtype=torch.uint8 if e4m3_out else torch.float16, device=device)
@@ -288,7 +297,7 @@ def run_ours(args) -> None:
 
     def fwd(o=out):
         bevpool.forward(m, depth, feat, wl.C, dtype=dt, depth_scale=wl.depth_scale, feat_scale=wl.feat_scale,
-                        out=o, capacity=cap, out_scale=out_scale)
+                        out=o, capacity=cap, out_scale=out_scale, feat_block=block)
 
     def build():
         bevpool.build_map(cells, *wl.dims(), wl.n_cells, out=m, workspace=ws, sync=False)
@@ -365,7 +374,7 @@ def run_ours(args) -> None:
     # One frame with its own geometry (bevpool_pool_frame: map build + forward,
     # no host sync) replayed from a CUDA graph, warm L2.
     frame_us = None
-    if not e4m3_out:
+    if not e4m3_out and wl.dtype != "nvfp4":
         try:
             fm = bevpool.ScatterMap.allocate(*wl.dims(), wl.n_cells, device)
             fout = torch.empty_like(out)
@@ -404,6 +413,8 @@ def run_ours(args) -> None:
         a.record(stream)
         depth.copy_(depth_h, non_blocking=True)
         feat.copy_(feat_h, non_blocking=True)
+        if block is not None:
+            block.copy_(block_h, non_blocking=True)
         fwd()
         out_h.copy_(out, non_blocking=True)
         b.record(stream)
@@ -412,6 +423,8 @@ def run_ours(args) -> None:
             e2e_ms.append(a.elapsed_time(b))
     e2e_us = max_over_ranks([statistics.mean(e2e_ms) * 1e3], world, device)[0]
     h2d = depth_h.numel() * depth_h.element_size() + feat_h.numel() * feat_h.element_size()
+    if block_h is not None:
+        h2d += block_h.numel()
     d2h = out_h.numel() * out_h.element_size()
 
     if rank != 0:

@@ -37,6 +37,7 @@ BEVPOOL_ERR_WORKSPACE = 4
 BEVPOOL_ERR_CUDA = 5
 BEVPOOL_F16 = 0
 BEVPOOL_E4M3 = 1
+BEVPOOL_NVFP4 = 2
 BEVPOOL_NOALLOC_MAX_FRUSTUM = 1 << 21
 
 _i32, _i64, _sz, _vp, _f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
@@ -61,6 +62,9 @@ _lib.bevpool_forward.restype = ctypes.c_int
 _lib.bevpool_forward_e4m3_out.argtypes = [ctypes.c_int, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _f32,
                                           _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp]
 _lib.bevpool_forward_e4m3_out.restype = ctypes.c_int
+_lib.bevpool_forward_nvfp4.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _f32, ctypes.c_int, _f32,
+                                       _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp]
+_lib.bevpool_forward_nvfp4.restype = ctypes.c_int
 _lib.bevpool_pool_frame.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _vp, _vp, _i32, _f32, _f32,
                                     _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]
 _lib.bevpool_pool_frame.restype = ctypes.c_int
@@ -134,6 +138,16 @@ def bevpool_forward_e4m3_out(dtype: int, depth: int, feat: int, NC: int, D: int,
     return _lib.bevpool_forward_e4m3_out(dtype, depth, feat, NC, D, H, W, C, depth_scale, feat_scale, out_scale,
                                          ranks_depth, ranks_feat, ranks_bev, interval_starts, interval_lengths,
                                          n_points, n_intervals, d_counts, n_cells, out, stream)
+
+
+def bevpool_forward_nvfp4(depth: int, feat: int, feat_block: int, NC: int, D: int, H: int, W: int, C: int,
+                          depth_scale: float, feat_scale: float, out_dtype: int, out_scale: float,
+                          ranks_depth: int, ranks_feat: int, ranks_bev: int, interval_starts: int,
+                          interval_lengths: int, n_points: int, n_intervals: int, d_counts: Optional[int],
+                          n_cells: int, out: int, stream: int) -> int:
+    return _lib.bevpool_forward_nvfp4(depth, feat, feat_block, NC, D, H, W, C, depth_scale, feat_scale, out_dtype,
+                                      out_scale, ranks_depth, ranks_feat, ranks_bev, interval_starts,
+                                      interval_lengths, n_points, n_intervals, d_counts, n_cells, out, stream)
 
 
 def bevpool_pool_frame(cell_ids: int, NC: int, D: int, H: int, W: int, n_cells: int, dtype: int, depth: int,
@@ -232,10 +246,12 @@ def build_map(cell_ids, NC: int, D: int, H: int, W: int, n_cells: int, *, out: O
 
 def forward(m: ScatterMap, depth, feat, C: int, *, dtype: int = BEVPOOL_F16, depth_scale: float = 1.0,
             feat_scale: float = 1.0, out=None, stream=None, capacity: Optional[tuple] = None,
-            out_scale: Optional[float] = None):
+            out_scale: Optional[float] = None, feat_block=None):
     """bevpool_forward over a map.  Returns the [n_cells, C] output tensor:
     fp16, or, when ``out_scale`` is given, uint8 E4M3 codes of value / out_scale
-    (bevpool_forward_e4m3_out).
+    (bevpool_forward_e4m3_out).  dtype BEVPOOL_NVFP4 takes the packed E2M1
+    features in ``feat`` and their E4M3 block scales in ``feat_block``
+    (bevpool_forward_nvfp4).
 
     If the map's host counts are unknown (built with sync=False), the device
     counts are used with ``capacity`` = (max points, max intervals) as bounds."""
@@ -252,7 +268,15 @@ def forward(m: ScatterMap, depth, feat, C: int, *, dtype: int = BEVPOOL_F16, dep
         dc = m.d_counts.data_ptr()
     maps = (m.ranks_depth.data_ptr(), m.ranks_feat.data_ptr(), m.ranks_bev.data_ptr(), m.interval_starts.data_ptr(),
             m.interval_lengths.data_ptr(), n_pts, n_int, dc, m.n_cells, out.data_ptr(), _stream(stream))
-    if out_scale is None:
+    if dtype == BEVPOOL_NVFP4:
+        if feat_block is None:
+            raise BevpoolError(BEVPOOL_ERR_INVALID_ARG, "NVFP4 features need feat_block")
+        st = bevpool_forward_nvfp4(depth.data_ptr(), feat.data_ptr(), feat_block.data_ptr(), m.NC, m.D, m.H, m.W, C,
+                                   depth_scale, feat_scale, BEVPOOL_F16 if out_scale is None else BEVPOOL_E4M3,
+                                   0.0 if out_scale is None else out_scale, *maps)
+        if st != BEVPOOL_OK:
+            raise BevpoolError(st, "bevpool_forward_nvfp4")
+    elif out_scale is None:
         st = bevpool_forward(dtype, depth.data_ptr(), feat.data_ptr(), m.NC, m.D, m.H, m.W, C, depth_scale,
                              feat_scale, *maps)
         if st != BEVPOOL_OK:

@@ -32,6 +32,14 @@ bool device_info(DeviceInfo *out) {
 }
 
 bool forward_supported(int dtype, int C) {
+    if (dtype == BEVPOOL_NVFP4) {
+        switch (C) {
+            case 64: case 80: case 96: case 128: case 160: case 192: case 256:
+                return true;
+            default:
+                return false;
+        }
+    }
     if (dtype != BEVPOOL_F16 && dtype != BEVPOOL_E4M3) return false;
     switch (C) {
         case 8: case 16: case 32: case 64: case 80: case 96: case 128: case 160: case 192: case 256:
@@ -200,15 +208,17 @@ namespace {
 
 // Shared body of the two forward entry points (fp16 output, or E4M3 output
 // codes of value / out_scale).
-bevpool_status forward_impl(bevpool_dtype dtype, const void *depth, const void *feat, int32_t NC, int32_t D,
-                            int32_t H, int32_t W, int32_t C, float depth_scale, float feat_scale, bool e4m3_out,
+bevpool_status forward_impl(bevpool_dtype dtype, const void *depth, const void *feat, const void *feat_block,
+                            int32_t NC, int32_t D, int32_t H, int32_t W, int32_t C, float depth_scale,
+                            float feat_scale, bool e4m3_out,
                             float out_scale, const int32_t *ranks_depth, const int32_t *ranks_feat,
                             const int32_t *ranks_bev, const int32_t *interval_starts,
                             const int32_t *interval_lengths, int32_t n_points, int32_t n_intervals,
                             const int32_t *d_counts, int32_t n_cells, void *out, void *stream) {
-    if (dtype != BEVPOOL_F16 && dtype != BEVPOOL_E4M3) return BEVPOOL_ERR_UNSUPPORTED;
+    if (dtype != BEVPOOL_F16 && dtype != BEVPOOL_E4M3 && dtype != BEVPOOL_NVFP4) return BEVPOOL_ERR_UNSUPPORTED;
     if (!forward_supported(static_cast<int>(dtype), C)) return BEVPOOL_ERR_UNSUPPORTED;
     if (e4m3_out && C % 16 != 0) return BEVPOOL_ERR_UNSUPPORTED;
+    if (dtype == BEVPOOL_NVFP4 && !feat_block) return BEVPOOL_ERR_INVALID_ARG;
     if (!frustum_ok(NC, D, H, W) || n_cells < 1) return BEVPOOL_ERR_INVALID_ARG;
     if (static_cast<int64_t>(n_cells) * C > INT32_MAX) return BEVPOOL_ERR_INVALID_ARG;
     const int64_t nf = static_cast<int64_t>(NC) * D * H * W;
@@ -232,6 +242,7 @@ bevpool_status forward_impl(bevpool_dtype dtype, const void *depth, const void *
     ForwardArgs a;
     a.depth = depth;
     a.feat = feat;
+    a.feat_block = feat_block;
     a.ranks_depth = ranks_depth;
     a.ranks_feat = ranks_feat;
     a.ranks_bev = ranks_bev;
@@ -250,15 +261,18 @@ bevpool_status forward_impl(bevpool_dtype dtype, const void *depth, const void *
     // forward touches do not fit comfortably in L2, stream the output past it.
     const int64_t eb = dtype == BEVPOOL_F16 ? 2 : 1;
     const int64_t ob = e4m3_out ? 1 : 2;
+    const int64_t feat_bytes = dtype == BEVPOOL_NVFP4 ? static_cast<int64_t>(a.n_feat_rows) * (C / 2 + C / 16)
+                                                      : static_cast<int64_t>(a.n_feat_rows) * C * eb;
     const int64_t footprint = static_cast<int64_t>(n_points) * 12 + static_cast<int64_t>(n_intervals) * 8 +
-                              nf * eb + static_cast<int64_t>(a.n_feat_rows) * C * eb +
-                              static_cast<int64_t>(n_cells) * C * ob;
+                              nf * eb + feat_bytes + static_cast<int64_t>(n_cells) * C * ob;
     a.streaming_stores = footprint > static_cast<int64_t>(info.l2_bytes) / 2 ? 1 : 0;
     a.sm_count = info.sm_count;
     a.out = out;
     a.stream = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (e4m3_out)
+    if (dtype == BEVPOOL_NVFP4)
+        e = e4m3_out ? launch_forward_nvfp4_e4m3out(a) : launch_forward_nvfp4(a);
+    else if (e4m3_out)
         e = dtype == BEVPOOL_F16 ? launch_forward_f16_e4m3out(a) : launch_forward_e4m3_e4m3out(a);
     else
         e = dtype == BEVPOOL_F16 ? launch_forward_f16(a) : launch_forward_e4m3(a);
@@ -273,7 +287,8 @@ bevpool_status bevpool_forward(bevpool_dtype dtype, const void *depth, const voi
                                const int32_t *interval_starts, const int32_t *interval_lengths,
                                int32_t n_points, int32_t n_intervals, const int32_t *d_counts, int32_t n_cells,
                                void *out, void *stream) {
-    return forward_impl(dtype, depth, feat, NC, D, H, W, C, depth_scale, feat_scale, false, 0.0f, ranks_depth,
+    if (dtype == BEVPOOL_NVFP4) return BEVPOOL_ERR_UNSUPPORTED;      // needs the block scales
+    return forward_impl(dtype, depth, feat, nullptr, NC, D, H, W, C, depth_scale, feat_scale, false, 0.0f, ranks_depth,
                         ranks_feat, ranks_bev, interval_starts, interval_lengths, n_points, n_intervals, d_counts,
                         n_cells, out, stream);
 }
@@ -285,9 +300,24 @@ bevpool_status bevpool_forward_e4m3_out(bevpool_dtype dtype, const void *depth, 
                                         const int32_t *interval_starts, const int32_t *interval_lengths,
                                         int32_t n_points, int32_t n_intervals, const int32_t *d_counts,
                                         int32_t n_cells, void *out, void *stream) {
-    return forward_impl(dtype, depth, feat, NC, D, H, W, C, depth_scale, feat_scale, true, out_scale, ranks_depth,
+    if (dtype == BEVPOOL_NVFP4) return BEVPOOL_ERR_UNSUPPORTED;      // needs the block scales
+    return forward_impl(dtype, depth, feat, nullptr, NC, D, H, W, C, depth_scale, feat_scale, true, out_scale,
+                        ranks_depth,
                         ranks_feat, ranks_bev, interval_starts, interval_lengths, n_points, n_intervals, d_counts,
                         n_cells, out, stream);
+}
+
+bevpool_status bevpool_forward_nvfp4(const void *depth, const void *feat, const void *feat_block, int32_t NC,
+                                     int32_t D, int32_t H, int32_t W, int32_t C, float depth_scale,
+                                     float feat_scale, bevpool_dtype out_dtype, float out_scale,
+                                     const int32_t *ranks_depth, const int32_t *ranks_feat,
+                                     const int32_t *ranks_bev, const int32_t *interval_starts,
+                                     const int32_t *interval_lengths, int32_t n_points, int32_t n_intervals,
+                                     const int32_t *d_counts, int32_t n_cells, void *out, void *stream) {
+    if (out_dtype != BEVPOOL_F16 && out_dtype != BEVPOOL_E4M3) return BEVPOOL_ERR_UNSUPPORTED;
+    return forward_impl(BEVPOOL_NVFP4, depth, feat, feat_block, NC, D, H, W, C, depth_scale, feat_scale,
+                        out_dtype == BEVPOOL_E4M3, out_scale, ranks_depth, ranks_feat, ranks_bev, interval_starts,
+                        interval_lengths, n_points, n_intervals, d_counts, n_cells, out, stream);
 }
 
 bevpool_status bevpool_pool_frame(const int32_t *cell_ids, int32_t NC, int32_t D, int32_t H, int32_t W,

@@ -123,6 +123,7 @@ cudaError_t launch_build_map_counting(const BuildMapArgs &a);
 // Forward (forward_f16.cu / forward_e4m3.cu).
 struct ForwardArgs {
     const void *depth, *feat;
+    const void *feat_block;   // NVFP4 block scales (else unused)
     const int32_t *ranks_depth, *ranks_feat, *ranks_bev;
     const int32_t *interval_starts, *interval_lengths;
     const int32_t *d_counts;
@@ -141,6 +142,8 @@ cudaError_t launch_forward_f16(const ForwardArgs &a);             // fp16 output
 cudaError_t launch_forward_e4m3(const ForwardArgs &a);
 cudaError_t launch_forward_f16_e4m3out(const ForwardArgs &a);     // E4M3 output (C % 16 == 0)
 cudaError_t launch_forward_e4m3_e4m3out(const ForwardArgs &a);
+cudaError_t launch_forward_nvfp4(const ForwardArgs &a);           // NVFP4 features, fp16 output
+cudaError_t launch_forward_nvfp4_e4m3out(const ForwardArgs &a);   // NVFP4 features, E4M3 output
 
 // Map validation (abi.cu).
 cudaError_t launch_validate_map(const int32_t *ranks_depth, const int32_t *ranks_feat,

@@ -59,6 +59,10 @@
 #define BEVPOOL_FWD_E4M3_BATCH16 5       // points in flight per owner for E4M3 rows read 16 bytes per lane (registers: 5 rows of 16 B next to 16 FP32 sums)
 #endif
 
+#ifndef BEVPOOL_FWD_NVFP4_BATCH
+#define BEVPOOL_FWD_NVFP4_BATCH 6        // points in flight per owner for NVFP4 rows (16 channels per lane)
+#endif
+
 #ifndef BEVPOOL_FMA_VARIANT
 #define BEVPOOL_FMA_VARIANT 1   // 0: convert to f32 + FFMA, 1: f16 x f16 + f32 FMA, 2: convert + packed f32x2 FMA
 #endif
@@ -67,6 +71,7 @@ namespace bevpool {
 
 constexpr int kDtypeF16 = 0;
 constexpr int kDtypeE4M3 = 1;
+constexpr int kDtypeNVFP4 = 2;   // E2M1 features with an E4M3 scale per 16 elements, E4M3 depth
 constexpr int kOutF16 = 0;     // output element: fp16 (round to nearest even)
 constexpr int kOutE4M3 = 1;    // output element: OCP E4M3 code (round to nearest even, saturating)
 constexpr int kFillCellsMin = 256;    // cells per fill CTA: a power of two in [min, max], chosen per call
@@ -83,26 +88,31 @@ constexpr int kFillCellsMax = 1024;
 
 template <int DT, int C>
 struct FwdShape {
-    static constexpr int EB = DT == kDtypeF16 ? 2 : 1;          // input bytes per element
-    static constexpr int ROWB = C * EB;                         // bytes per feature row
+    static constexpr bool NV = DT == kDtypeNVFP4;
+    static constexpr int EB = DT == kDtypeF16 ? 2 : 1;          // input bytes per element (E4M3)
+    static constexpr int ROWB = NV ? C / 2 : C * EB;            // bytes per feature row
     static constexpr int LANE_BYTES = DT == kDtypeF16 ? BEVPOOL_FWD_LANE_BYTES : BEVPOOL_FWD_E4M3_LANE_BYTES;
-    static constexpr int VB = ROWB >= 4 * LANE_BYTES && ROWB % LANE_BYTES == 0
-                                  ? LANE_BYTES
-                                  : (ROWB >= 64 ? 16 : ROWB / 4);   // bytes per lane (>= 4 lanes per owner)
+    static constexpr int VB = NV ? 8                            // NVFP4: one 16-element block per lane
+                              : (ROWB >= 4 * LANE_BYTES && ROWB % LANE_BYTES == 0
+                                     ? LANE_BYTES
+                                     : (ROWB >= 64 ? 16 : ROWB / 4));   // bytes per lane (>= 4 lanes per owner)
     static constexpr int LPO = ROWB / VB;                       // lanes per owner
-    static constexpr int EPL = VB / EB;                         // channels per lane
+    static constexpr int EPL = NV ? 16 : VB / EB;               // channels per lane
     static constexpr int OPW = 32 / LPO;                        // owners per warp
     static constexpr int OWNERS = kWarps * OPW;                 // owners per CTA
-    static constexpr int BATCH_CFG = VB >= 32 ? 4 : ((DT == kDtypeF16 || VB < 16) ? BEVPOOL_FWD_BATCH : BEVPOOL_FWD_E4M3_BATCH16);
+    static constexpr int BATCH_CFG = NV ? BEVPOOL_FWD_NVFP4_BATCH
+                                        : (VB >= 32 ? 4 : ((DT == kDtypeF16 || VB < 16) ? BEVPOOL_FWD_BATCH
+                                                                                        : BEVPOOL_FWD_E4M3_BATCH16));
     static constexpr int BATCH = BATCH_CFG < LPO ? BATCH_CFG : LPO;   // points in flight per owner (<= LPO)
     static_assert(ROWB % VB == 0 && (VB == 2 || VB == 4 || VB == 8 || VB == 16 || VB == 32), "bad vector width");
     static_assert(LPO >= 4 && LPO <= 32, "bad lane mapping");
-    static_assert(C % 8 == 0, "C must be a multiple of 8");
+    static_assert(C % 8 == 0 && (!NV || C % 16 == 0), "C must be a multiple of 8 (16 for NVFP4)");
 };
 
 struct FwdParams {
     const void *depth;
     const void *feat;
+    const unsigned char *feat_block;   // NVFP4: E4M3 scale of each 16-element block, [rows, C/16]
     const int32_t *ranks_depth;
     const int32_t *ranks_feat;
     const int32_t *ranks_bev;
@@ -193,6 +203,33 @@ __device__ __forceinline__ void fma_h2(float &a0, float &a1, unsigned short d, u
 #endif
 }
 
+// acc[0..8) += d * (eight E2M1 codes of w, lowest nibble first): each byte
+// widens to two fp16 values in one conversion (exact), then FP32 FMAs.
+__device__ __forceinline__ void fma_e2m1x8(float *acc, unsigned short d, uint32_t w) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t.reg .b32 p0, p1, p2, p3;\n\t"
+        ".reg .f16 h0, h1, h2, h3, h4, h5, h6, h7;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %8;\n\t"
+        "cvt.rn.f16x2.e2m1x2 p0, b0;\n\tcvt.rn.f16x2.e2m1x2 p1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 p2, b2;\n\tcvt.rn.f16x2.e2m1x2 p3, b3;\n\t"
+        "mov.b32 {h0, h1}, p0;\n\tmov.b32 {h2, h3}, p1;\n\tmov.b32 {h4, h5}, p2;\n\tmov.b32 {h6, h7}, p3;\n\t"
+        "fma.rn.f32.f16 %0, %9, h0, %0;\n\tfma.rn.f32.f16 %1, %9, h1, %1;\n\t"
+        "fma.rn.f32.f16 %2, %9, h2, %2;\n\tfma.rn.f32.f16 %3, %9, h3, %3;\n\t"
+        "fma.rn.f32.f16 %4, %9, h4, %4;\n\tfma.rn.f32.f16 %5, %9, h5, %5;\n\t"
+        "fma.rn.f32.f16 %6, %9, h6, %6;\n\tfma.rn.f32.f16 %7, %9, h7, %7;\n\t}"
+        : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3]), "+f"(acc[4]), "+f"(acc[5]), "+f"(acc[6]),
+          "+f"(acc[7])
+        : "r"(w), "h"(d));
+}
+
+// Product of two fp16 values given as bits.  Used for depth x block scale of
+// NVFP4 rows: both are E4M3 values, so the product (at most 8 significant
+// bits, magnitude between 2^-18 and 448) is exact in fp16.
+__device__ __forceinline__ unsigned short mul_f16_bits(unsigned short a, unsigned short b) {
+    unsigned short r;
+    asm("mul.rn.f16 %0, %1, %2;" : "=h"(r) : "h"(a), "h"(b));
+    return r;
+}
+
 // acc[0..4) += d * (four E4M3 codes of w, lowest byte first): each pair of
 // codes widens to two fp16 values in one conversion (exact), then FP32 FMAs.
 __device__ __forceinline__ void fma_e4m3x4(float *acc, unsigned short d, uint32_t w) {
@@ -209,7 +246,10 @@ __device__ __forceinline__ void fma_e4m3x4(float *acc, unsigned short d, uint32_
 // acc[0 .. EPL) += d * decode(raw)
 template <int DT, int VB>
 __device__ __forceinline__ void fma_vec(float *acc, unsigned short d, const RawVec<VB> &raw) {
-    if constexpr (DT == kDtypeF16) {
+    if constexpr (DT == kDtypeNVFP4) {
+#pragma unroll
+        for (int i = 0; i < VB / 4; ++i) fma_e2m1x8(acc + 8 * i, d, raw.w[i]);
+    } else if constexpr (DT == kDtypeF16) {
         if constexpr (VB == 2) {
             __half_raw hr;
             hr.x = static_cast<unsigned short>(raw.w[0]);
@@ -464,6 +504,11 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
                 if (a[kk] >= 0) {
                     d[kk] = load_depth_h<DT>(p.depth, a[kk]);
                     f[kk] = load_vec<S::VB>(featp + static_cast<int64_t>(b[kk]) * S::ROWB);
+                    if constexpr (S::NV) {                   // depth x the lane's block scale (exact in fp16)
+                        const unsigned char sc = __ldg(p.feat_block + static_cast<int64_t>(b[kk]) * (C / 16) + ol);
+                        const __half_raw sh = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sc), __NV_E4M3);
+                        d[kk] = mul_f16_bits(d[kk], sh.x);
+                    }
                 } else {                                     // past the share, or an invalid rank: adds +0
                     d[kk] = 0;
 #pragma unroll
@@ -583,6 +628,7 @@ cudaError_t launch_forward_t(const ForwardArgs &a) {
     FwdParams p;
     p.depth = a.depth;
     p.feat = a.feat;
+    p.feat_block = static_cast<const unsigned char *>(a.feat_block);
     p.ranks_depth = a.ranks_depth;
     p.ranks_feat = a.ranks_feat;
     p.ranks_bev = a.ranks_bev;

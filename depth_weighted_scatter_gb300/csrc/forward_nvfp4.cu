@@ -1,0 +1,20 @@
+// forward_nvfp4.cu -- instantiates the forward kernel for NVFP4 features and fp16 output,
+// one entry point per channel count (compiled in its own unit to build in parallel).
+#include "forward_impl.cuh"
+
+namespace bevpool {
+
+cudaError_t launch_forward_nvfp4(const ForwardArgs &a) {
+    switch (a.C) {
+        case 64: return launch_forward_t<kDtypeNVFP4, 64, kOutF16>(a);
+        case 80: return launch_forward_t<kDtypeNVFP4, 80, kOutF16>(a);
+        case 96: return launch_forward_t<kDtypeNVFP4, 96, kOutF16>(a);
+        case 128: return launch_forward_t<kDtypeNVFP4, 128, kOutF16>(a);
+        case 160: return launch_forward_t<kDtypeNVFP4, 160, kOutF16>(a);
+        case 192: return launch_forward_t<kDtypeNVFP4, 192, kOutF16>(a);
+        case 256: return launch_forward_t<kDtypeNVFP4, 256, kOutF16>(a);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace bevpool

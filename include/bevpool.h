@@ -63,7 +63,9 @@ typedef enum bevpool_status {
 
 typedef enum bevpool_dtype {
     BEVPOOL_F16 = 0,   /* depth and feat are IEEE binary16                         */
-    BEVPOOL_E4M3 = 1   /* depth and feat are OCP FP8 E4M3 codes, one scale each    */
+    BEVPOOL_E4M3 = 1,  /* depth and feat are OCP FP8 E4M3 codes, one scale each    */
+    BEVPOOL_NVFP4 = 2  /* feat NVFP4 (E2M1 + E4M3 block scales), depth E4M3:
+                          bevpool_forward_nvfp4 only                             */
 } bevpool_dtype;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -76,7 +78,8 @@ BEVPOOL_API int32_t bevpool_version(void);
  * (all devices, all streams).  Used to count launches in a timed region. */
 BEVPOOL_API int64_t bevpool_kernel_launches(void);
 
-/* Whether channel count C has a compiled forward kernel for dtype (1 / 0). */
+/* Whether channel count C has a compiled forward kernel for dtype (1 / 0);
+ * for BEVPOOL_NVFP4 it answers for bevpool_forward_nvfp4. */
 BEVPOOL_API int32_t bevpool_forward_supported(bevpool_dtype dtype, int32_t C);
 
 /*
@@ -230,6 +233,38 @@ BEVPOOL_API bevpool_status bevpool_forward_e4m3_out(bevpool_dtype dtype, const v
                                         const int32_t *interval_lengths, int32_t n_points,
                                         int32_t n_intervals, const int32_t *d_counts, int32_t n_cells,
                                         void *out, void *stream);
+
+/*
+ * The forward with NVFP4 features, the experiment of section "Map the
+ * algorithm to hardware": camera features stored as OCP E2M1 (4-bit)
+ * elements with one E4M3 scale per 16 elements, depth kept in E4M3.  Feature
+ * value c of row r:
+ *     e2m1(nibble c of feat row r) * e4m3(feat_block[r * C/16 + c/16]) * feat_scale
+ * with element 2i in the low nibble of byte i (a row is C/2 bytes); depth
+ * value = e4m3(depth[p]) * depth_scale.  The sum and the rest of the
+ * semantics are those of bevpool_forward; out_dtype BEVPOOL_F16 stores fp16
+ * rows, BEVPOOL_E4M3 stores E4M3 codes of value / out_scale as
+ * bevpool_forward_e4m3_out does (out_scale is ignored for fp16).
+ *
+ *   depth             device, [NC, D, H, W] E4M3 codes.
+ *   feat              device, [NC*H*W, C/2] bytes of E2M1 pairs, 16-byte aligned.
+ *   feat_block        device, [NC*H*W, C/16] E4M3 block scales.
+ *   C                 64, 80, 96, 128, 160, 192 or 256 (one 16-element block
+ *                     per lane, at least four lanes per row).
+ *
+ * Each depth code times each block scale is formed in fp16 (exact for E4M3
+ * values), so their product must stay within the fp16 range (|product| <=
+ * 65504); it does when the depth codes lie in [-1, 1], as when depth_scale =
+ * max|depth|.  The pages report this format slower than FP8 for the
+ * scatter-reduce; it is here to confirm that on this GPU.
+ */
+BEVPOOL_API bevpool_status bevpool_forward_nvfp4(const void *depth, const void *feat, const void *feat_block,
+                                     int32_t NC, int32_t D, int32_t H, int32_t W, int32_t C,
+                                     float depth_scale, float feat_scale, bevpool_dtype out_dtype,
+                                     float out_scale, const int32_t *ranks_depth, const int32_t *ranks_feat,
+                                     const int32_t *ranks_bev, const int32_t *interval_starts,
+                                     const int32_t *interval_lengths, int32_t n_points, int32_t n_intervals,
+                                     const int32_t *d_counts, int32_t n_cells, void *out, void *stream);
 
 /*
  * One frame with its own geometry: bevpool_build_map (no host

@@ -146,3 +146,17 @@ def test_pool_frame_rejects_bad_arguments(bp):
                    dict(depth_scale=float("inf"))]:
         assert bp.bevpool_pool_frame(**{**args, **change}) == bp.BEVPOOL_ERR_INVALID_ARG, change
     assert bp.bevpool_pool_frame(**{**args, "workspace_bytes": ws - 1}) == bp.BEVPOOL_ERR_WORKSPACE
+
+
+def test_forward_nvfp4_rejects_bad_arguments(bp):
+    assert bp.bevpool_forward_supported(bp.BEVPOOL_NVFP4, 80)
+    assert not bp.bevpool_forward_supported(bp.BEVPOOL_NVFP4, 32)
+    args = dict(depth=FAKE, feat=FAKE, feat_block=FAKE, NC=2, D=3, H=4, W=5, C=80, depth_scale=1.0, feat_scale=1.0,
+                out_dtype=bp.BEVPOOL_F16, out_scale=0.0, ranks_depth=FAKE, ranks_feat=FAKE, ranks_bev=FAKE,
+                interval_starts=FAKE, interval_lengths=FAKE, n_points=50, n_intervals=20, d_counts=None, n_cells=30,
+                out=FAKE, stream=0)
+    for change in [dict(C=32), dict(C=8), dict(out_dtype=bp.BEVPOOL_NVFP4)]:
+        assert bp.bevpool_forward_nvfp4(**{**args, **change}) == bp.BEVPOOL_ERR_UNSUPPORTED, change
+    for change in [dict(feat_block=0), dict(feat=FAKE + 8), dict(out_dtype=bp.BEVPOOL_E4M3, out_scale=0.0),
+                   dict(NC=0)]:
+        assert bp.bevpool_forward_nvfp4(**{**args, **change}) == bp.BEVPOOL_ERR_INVALID_ARG, change
