@@ -59,6 +59,9 @@
 #define BEVPOOL_FWD_E4M3_BATCH16 5       // points in flight per owner for E4M3 rows read 16 bytes per lane (registers: 5 rows of 16 B next to 16 FP32 sums)
 #endif
 
+#ifndef BEVPOOL_FWD_BATCH32
+#define BEVPOOL_FWD_BATCH32 4            // points in flight per owner for rows read 32 bytes per lane
+#endif
 #ifndef BEVPOOL_FWD_NVFP4_BATCH
 #define BEVPOOL_FWD_NVFP4_BATCH 6        // points in flight per owner for NVFP4 rows (16 channels per lane)
 #endif
@@ -101,7 +104,7 @@ struct FwdShape {
     static constexpr int OPW = 32 / LPO;                        // owners per warp
     static constexpr int OWNERS = kWarps * OPW;                 // owners per CTA
     static constexpr int BATCH_CFG = NV ? BEVPOOL_FWD_NVFP4_BATCH
-                                        : (VB >= 32 ? 4 : ((DT == kDtypeF16 || VB < 16) ? BEVPOOL_FWD_BATCH
+                                        : (VB >= 32 ? BEVPOOL_FWD_BATCH32 : ((DT == kDtypeF16 || VB < 16) ? BEVPOOL_FWD_BATCH
                                                                                         : BEVPOOL_FWD_E4M3_BATCH16));
     static constexpr int BATCH = BATCH_CFG < LPO ? BATCH_CFG : LPO;   // points in flight per owner (<= LPO)
     static_assert(ROWB % VB == 0 && (VB == 2 || VB == 4 || VB == 8 || VB == 16 || VB == 32), "bad vector width");
