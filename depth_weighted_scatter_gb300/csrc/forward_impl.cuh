@@ -59,6 +59,9 @@
 #define BEVPOOL_FWD_E4M3_BATCH16 5       // points in flight per owner for E4M3 rows read 16 bytes per lane (registers: 5 rows of 16 B next to 16 FP32 sums)
 #endif
 
+#ifndef BEVPOOL_FWD_DEPTH_SHFL
+#define BEVPOOL_FWD_DEPTH_SHFL 2         // who loads a point's depth: 0 every lane of the owner, 1 the lane that
+#endif                                   // fetched the point's ranks (a shuffle hands it out), 2 that for FP8 rows
 #ifndef BEVPOOL_FWD_BATCH32
 #define BEVPOOL_FWD_BATCH32 4            // points in flight per owner for rows read 32 bytes per lane
 #endif
@@ -88,6 +91,11 @@ constexpr int kFillCellsMax = 1024;
 #ifndef BEVPOOL_FWD_CTAS_PER_SM_DRAM
 #define BEVPOOL_FWD_CTAS_PER_SM_DRAM 3
 #endif
+
+// Whether the owner's fetch lane loads each point's depth (one load per point,
+// one shuffle per lane) instead of every lane loading it.
+template <int DT>
+constexpr bool kDepthShfl = BEVPOOL_FWD_DEPTH_SHFL == 1 || (BEVPOOL_FWD_DEPTH_SHFL == 2 && DT != 0);
 
 template <int DT, int C>
 struct FwdShape {
@@ -494,28 +502,59 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
             const bool is_end = ol < S::BATCH && j < end &&
                                 (j + 1 == P || rc != (ol + 1 < S::BATCH ? succ_in : succ_nx));
             const unsigned ends = __ballot_sync(gmask, is_end) >> lane0;
-            int a[S::BATCH], b[S::BATCH];
-#pragma unroll
-            for (int kk = 0; kk < S::BATCH; ++kk) {
-                a[kk] = __shfl_sync(gmask, rd, lane0 + kk);
-                b[kk] = __shfl_sync(gmask, rf, lane0 + kk);
-            }
             unsigned short d[S::BATCH];
             RawVec<S::VB> f[S::BATCH];
+            if constexpr (kDepthShfl<DT>) {
+                // lane kk loads the depth of point kk; shuffles hand depth and row to the owner's lanes
+                const int dv = rd >= 0 ? static_cast<int>(load_depth_h<DT>(p.depth, rd)) : 0;
+                int b[S::BATCH];
 #pragma unroll
-            for (int kk = 0; kk < S::BATCH; ++kk) {
-                if (a[kk] >= 0) {
-                    d[kk] = load_depth_h<DT>(p.depth, a[kk]);
-                    f[kk] = load_vec<S::VB>(featp + static_cast<int64_t>(b[kk]) * S::ROWB);
-                    if constexpr (S::NV) {                   // depth x the lane's block scale (exact in fp16)
-                        const unsigned char sc = __ldg(p.feat_block + static_cast<int64_t>(b[kk]) * (C / 16) + ol);
-                        const __half_raw sh = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sc), __NV_E4M3);
-                        d[kk] = mul_f16_bits(d[kk], sh.x);
+                for (int kk = 0; kk < S::BATCH; ++kk) b[kk] = __shfl_sync(gmask, rf, lane0 + kk);
+                [[maybe_unused]] unsigned short sh[S::BATCH];
+#pragma unroll
+                for (int kk = 0; kk < S::BATCH; ++kk) {
+                    if (b[kk] >= 0) {
+                        f[kk] = load_vec<S::VB>(featp + static_cast<int64_t>(b[kk]) * S::ROWB);
+                        if constexpr (S::NV) {
+                            const unsigned char sc =
+                                __ldg(p.feat_block + static_cast<int64_t>(b[kk]) * (C / 16) + ol);
+                            sh[kk] = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sc), __NV_E4M3).x;
+                        }
+                    } else {                                     // past the share, or an invalid rank: adds +0
+#pragma unroll
+                        for (int i = 0; i < RawVec<S::VB>::NW; ++i) f[kk].w[i] = 0u;
+                        if constexpr (S::NV) sh[kk] = 0;
                     }
-                } else {                                     // past the share, or an invalid rank: adds +0
-                    d[kk] = 0;
+                }
 #pragma unroll
-                    for (int i = 0; i < RawVec<S::VB>::NW; ++i) f[kk].w[i] = 0u;
+                for (int kk = 0; kk < S::BATCH; ++kk) {
+                    d[kk] = static_cast<unsigned short>(__shfl_sync(gmask, dv, lane0 + kk));
+                    if constexpr (S::NV) d[kk] = mul_f16_bits(d[kk], sh[kk]);   // depth x block scale (exact in fp16)
+                }
+            } else {
+                int a[S::BATCH], b[S::BATCH];
+#pragma unroll
+                for (int kk = 0; kk < S::BATCH; ++kk) {
+                    a[kk] = __shfl_sync(gmask, rd, lane0 + kk);
+                    b[kk] = __shfl_sync(gmask, rf, lane0 + kk);
+                }
+#pragma unroll
+                for (int kk = 0; kk < S::BATCH; ++kk) {
+                    if (a[kk] >= 0) {
+                        d[kk] = load_depth_h<DT>(p.depth, a[kk]);
+                        f[kk] = load_vec<S::VB>(featp + static_cast<int64_t>(b[kk]) * S::ROWB);
+                        if constexpr (S::NV) {                   // depth x the lane's block scale (exact in fp16)
+                            const unsigned char sc =
+                                __ldg(p.feat_block + static_cast<int64_t>(b[kk]) * (C / 16) + ol);
+                            const __half_raw sh =
+                                __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sc), __NV_E4M3);
+                            d[kk] = mul_f16_bits(d[kk], sh.x);
+                        }
+                    } else {                                     // past the share, or an invalid rank: adds +0
+                        d[kk] = 0;
+#pragma unroll
+                        for (int i = 0; i < RawVec<S::VB>::NW; ++i) f[kk].w[i] = 0u;
+                    }
                 }
             }
 #pragma unroll
