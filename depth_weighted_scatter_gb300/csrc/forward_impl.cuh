@@ -41,36 +41,40 @@
 
 #include "bevpool_internal.cuh"
 
-#ifndef BEVPOOL_FWD_BATCH
-#define BEVPOOL_FWD_BATCH 8     // points in flight per owner (fp16, and E4M3 with narrow lanes)
-#endif
+// Launch and inner-loop constants, chosen by measurement on GB300 (the design
+// notes list what else was tried); each can be overridden with -D.
 #ifndef BEVPOOL_FWD_MIN_CTAS
-#define BEVPOOL_FWD_MIN_CTAS 3  // resident CTAs per SM the register budget is sized for
+#define BEVPOOL_FWD_MIN_CTAS 3            // resident CTAs per SM the register budget (80) is sized for
 #endif
-
 #ifndef BEVPOOL_FWD_LANE_BYTES
-#define BEVPOOL_FWD_LANE_BYTES 16   // bytes of a feature row each lane loads (16 or 32) for wide rows
+#define BEVPOOL_FWD_LANE_BYTES 16         // bytes of an fp16 feature row one lane loads (16 or 32)
 #endif
-
 #ifndef BEVPOOL_FWD_E4M3_LANE_BYTES
-#define BEVPOOL_FWD_E4M3_LANE_BYTES 16   // bytes of an E4M3 feature row each lane loads
+#define BEVPOOL_FWD_E4M3_LANE_BYTES 16    // bytes of an E4M3 feature row one lane loads
+#endif
+#ifndef BEVPOOL_FWD_BATCH
+#define BEVPOOL_FWD_BATCH 8               // points in flight per owner: fp16 rows, and E4M3 rows under 16 B a lane
 #endif
 #ifndef BEVPOOL_FWD_E4M3_BATCH16
-#define BEVPOOL_FWD_E4M3_BATCH16 5       // points in flight per owner for E4M3 rows read 16 bytes per lane (registers: 5 rows of 16 B next to 16 FP32 sums)
+#define BEVPOOL_FWD_E4M3_BATCH16 5        // E4M3 rows at 16 B a lane (5 rows of 16 B beside 16 FP32 sums)
 #endif
-
-#ifndef BEVPOOL_FWD_DEPTH_SHFL
-#define BEVPOOL_FWD_DEPTH_SHFL 2         // who loads a point's depth: 0 every lane of the owner, 1 the lane that
-#endif                                   // fetched the point's ranks (a shuffle hands it out), 2 that for FP8 rows
 #ifndef BEVPOOL_FWD_BATCH32
-#define BEVPOOL_FWD_BATCH32 4            // points in flight per owner for rows read 32 bytes per lane
+#define BEVPOOL_FWD_BATCH32 4             // rows at 32 B a lane
 #endif
 #ifndef BEVPOOL_FWD_NVFP4_BATCH
-#define BEVPOOL_FWD_NVFP4_BATCH 6        // points in flight per owner for NVFP4 rows (16 channels per lane)
+#define BEVPOOL_FWD_NVFP4_BATCH 6         // NVFP4 rows (one 16-element block a lane)
 #endif
-
-#ifndef BEVPOOL_FMA_VARIANT
-#define BEVPOOL_FMA_VARIANT 1   // 0: convert to f32 + FFMA, 1: f16 x f16 + f32 FMA, 2: convert + packed f32x2 FMA
+#ifndef BEVPOOL_FWD_DEPTH_SHFL
+#define BEVPOOL_FWD_DEPTH_SHFL 2          // who loads a point's depth: 0 every lane of the owner, 1 the lane
+#endif                                    // that fetched its ranks (a shuffle hands it out), 2 that for FP8 rows
+// Compute CTAs per SM (one wave of them): with the output resident in L2,
+// two, leaving a slot for fill CTAs to run alongside; when the output streams
+// to DRAM, three (the gathers need the issue slots more than the fills).
+#ifndef BEVPOOL_FWD_CTAS_PER_SM_L2
+#define BEVPOOL_FWD_CTAS_PER_SM_L2 2
+#endif
+#ifndef BEVPOOL_FWD_CTAS_PER_SM_DRAM
+#define BEVPOOL_FWD_CTAS_PER_SM_DRAM 3
 #endif
 
 namespace bevpool {
@@ -82,15 +86,6 @@ constexpr int kOutF16 = 0;     // output element: fp16 (round to nearest even)
 constexpr int kOutE4M3 = 1;    // output element: OCP E4M3 code (round to nearest even, saturating)
 constexpr int kFillCellsMin = 256;    // cells per fill CTA: a power of two in [min, max], chosen per call
 constexpr int kFillCellsMax = 1024;
-// Compute CTAs per SM (one wave of them): with the output resident in L2,
-// two, leaving a slot for fill CTAs to run alongside; when the output streams
-// to DRAM, three (the gathers need the issue slots more than the fills).
-#ifndef BEVPOOL_FWD_CTAS_PER_SM_L2
-#define BEVPOOL_FWD_CTAS_PER_SM_L2 2
-#endif
-#ifndef BEVPOOL_FWD_CTAS_PER_SM_DRAM
-#define BEVPOOL_FWD_CTAS_PER_SM_DRAM 3
-#endif
 
 // Whether the owner's fetch lane loads each point's depth (one load per point,
 // one shuffle per lane) instead of every lane loading it.
@@ -111,9 +106,10 @@ struct FwdShape {
     static constexpr int EPL = NV ? 16 : VB / EB;               // channels per lane
     static constexpr int OPW = 32 / LPO;                        // owners per warp
     static constexpr int OWNERS = kWarps * OPW;                 // owners per CTA
-    static constexpr int BATCH_CFG = NV ? BEVPOOL_FWD_NVFP4_BATCH
-                                        : (VB >= 32 ? BEVPOOL_FWD_BATCH32 : ((DT == kDtypeF16 || VB < 16) ? BEVPOOL_FWD_BATCH
-                                                                                        : BEVPOOL_FWD_E4M3_BATCH16));
+    static constexpr int BATCH_CFG = NV                                  ? BEVPOOL_FWD_NVFP4_BATCH
+                                     : VB >= 32                          ? BEVPOOL_FWD_BATCH32
+                                     : (DT == kDtypeF16 || VB < 16)      ? BEVPOOL_FWD_BATCH
+                                                                         : BEVPOOL_FWD_E4M3_BATCH16;
     static constexpr int BATCH = BATCH_CFG < LPO ? BATCH_CFG : LPO;   // points in flight per owner (<= LPO)
     static_assert(ROWB % VB == 0 && (VB == 2 || VB == 4 || VB == 8 || VB == 16 || VB == 32), "bad vector width");
     static_assert(LPO >= 4 && LPO <= 32, "bad lane mapping");
@@ -186,32 +182,14 @@ __device__ __forceinline__ RawVec<VB> load_vec(const unsigned char *p) {
     return r;
 }
 
-// acc[0], acc[1] += d * (lo, hi) for one packed pair of fp16 values.
+// acc[0], acc[1] += d * (lo, hi) for one packed pair of fp16 values: FP32
+// FMAs taking the fp16 operands directly (f16 x f16 products are exact in
+// FP32).  Measured faster here than widening to f32 first, with or without
+// packed f32x2 FMAs.
 __device__ __forceinline__ void fma_h2(float &a0, float &a1, unsigned short d, uint32_t pair) {
-#if BEVPOOL_FMA_VARIANT == 1
     asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
         "fma.rn.f32.f16 %0, %3, lo, %0;\n\tfma.rn.f32.f16 %1, %3, hi, %1;\n\t}"
         : "+f"(a0), "+f"(a1) : "r"(pair), "h"(d));
-#else
-    __half2_raw hr;
-    hr.x = static_cast<unsigned short>(pair & 0xffffu);
-    hr.y = static_cast<unsigned short>(pair >> 16);
-    const float2 f = __half22float2(__half2(hr));
-    __half_raw dr;
-    dr.x = d;
-    const float df = __half2float(__half(dr));
-#if BEVPOOL_FMA_VARIANT == 2
-    unsigned long long acc, fv, dv;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(fv) : "f"(f.x), "f"(f.y));
-    asm("mov.b64 %0, {%1, %1};" : "=l"(dv) : "f"(df));
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(dv), "l"(fv));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
-#else
-    a0 = fmaf(df, f.x, a0);
-    a1 = fmaf(df, f.y, a1);
-#endif
-#endif
 }
 
 // acc[0..8) += d * (eight E2M1 codes of w, lowest nibble first): each byte
@@ -304,8 +282,8 @@ __device__ __forceinline__ void store_row_part(unsigned char *dst, const float *
         if constexpr (NW % 4 == 0) {
 #pragma unroll
             for (int q = 0; q < NW / 4; ++q)
-                store_vec(reinterpret_cast<uint4 *>(dst) + q, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]),
-                          streaming);
+                store_vec(reinterpret_cast<uint4 *>(dst) + q,
+                          make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]), streaming);
         } else if constexpr (NW == 2) {
             store_vec(reinterpret_cast<uint2 *>(dst), make_uint2(w[0], w[1]), streaming);
         } else {
@@ -326,8 +304,8 @@ __device__ __forceinline__ void store_row_part(unsigned char *dst, const float *
         if constexpr (NW % 4 == 0) {
 #pragma unroll
             for (int q = 0; q < NW / 4; ++q)
-                store_vec(reinterpret_cast<uint4 *>(dst) + q, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]),
-                          streaming);
+                store_vec(reinterpret_cast<uint4 *>(dst) + q,
+                          make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]), streaming);
         } else if constexpr (NW == 2) {
             store_vec(reinterpret_cast<uint2 *>(dst), make_uint2(w[0], w[1]), streaming);
         } else {
@@ -697,8 +675,8 @@ cudaError_t launch_forward_t(const ForwardArgs &a) {
     // Fill tiles: about four fill CTAs per SM (each costs a dependent search
     // before its stores, so large grids take larger tiles).
     int fill_cells = kFillCellsMin;
-    while (fill_cells < kFillCellsMax && a.n_cells > static_cast<int64_t>(fill_cells) * 4 * (a.sm_count > 0 ? a.sm_count : 148))
-        fill_cells *= 2;
+    const int64_t sms = a.sm_count > 0 ? a.sm_count : 148;
+    while (fill_cells < kFillCellsMax && a.n_cells > static_cast<int64_t>(fill_cells) * 4 * sms) fill_cells *= 2;
     p.fill_cells = fill_cells;
     p.n_fill = static_cast<int>(div_up(a.n_cells, fill_cells));
     p.out = static_cast<unsigned char *>(a.out);
