@@ -83,6 +83,8 @@ size_t carve(void *base, int64_t nf, int32_t n_cells, CountWs *ws) {
 
 __global__ void __launch_bounds__(kThreads) k_zero(int32_t *__restrict__ count, int32_t n_cells,
                                                    int32_t *__restrict__ invalid, int32_t *__restrict__ lists) {
+    grid_dep_wait();
+    grid_dep_allow();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n_cells; i += stride)
         count[i] = 0;
@@ -114,6 +116,8 @@ __device__ __forceinline__ void load_block(const int32_t *__restrict__ cell_ids,
 __global__ void __launch_bounds__(kThreads)
 k_count_cells(const int32_t *__restrict__ cell_ids, int64_t nf, int32_t n_cells, bool vec,
               int32_t *__restrict__ count, int32_t *__restrict__ invalid) {
+    grid_dep_wait();
+    grid_dep_allow();
     __shared__ long long red[kWarps];
     const int64_t first = static_cast<int64_t>(blockIdx.x) * kTile + static_cast<int64_t>(threadIdx.x) * kItems;
     int c[kItems];
@@ -133,6 +137,8 @@ k_count_cells(const int32_t *__restrict__ cell_ids, int64_t nf, int32_t n_cells,
 __global__ void __launch_bounds__(kThreads)
 k_tile_sums(const int32_t *__restrict__ count, int32_t n_cells, int32_t *__restrict__ tile_cnt,
             int32_t *__restrict__ tile_nz) {
+    grid_dep_wait();
+    grid_dep_allow();
     __shared__ long long red[kWarps];
     const int64_t base = static_cast<int64_t>(blockIdx.x) * kCellTile;
     int cnt = 0, nz = 0;
@@ -159,6 +165,8 @@ k_offsets(const int32_t *__restrict__ count, int32_t n_cells, const int32_t *__r
           const int32_t *__restrict__ tile_nz, int32_t *__restrict__ offset, int32_t *__restrict__ starts,
           int32_t *__restrict__ lengths, int32_t *__restrict__ icell, const int32_t *__restrict__ invalid,
           int32_t *__restrict__ d_counts) {
+    grid_dep_wait();
+    grid_dep_allow();
     __shared__ long long red[kWarps];
     __shared__ int scratch[kWarps + 1];
     const int b = blockIdx.x;
@@ -204,6 +212,8 @@ k_offsets(const int32_t *__restrict__ count, int32_t n_cells, const int32_t *__r
 __global__ void __launch_bounds__(kThreads)
 k_scatter(const int32_t *__restrict__ cell_ids, int64_t nf, int32_t n_cells, bool vec,
           int32_t *__restrict__ cursor, int32_t *__restrict__ tmp_p) {
+    grid_dep_wait();
+    grid_dep_allow();
     const int64_t first = static_cast<int64_t>(blockIdx.x) * kTile + static_cast<int64_t>(threadIdx.x) * kItems;
     int c[kItems];
     load_block(cell_ids, nf, vec, first, c);
@@ -341,6 +351,8 @@ k_sort_runs(const int32_t *__restrict__ tmp_p, const int32_t *__restrict__ start
             const int32_t *__restrict__ lengths, const int32_t *__restrict__ icell,
             const int32_t *__restrict__ d_counts, int32_t *__restrict__ lists, int32_t *__restrict__ mid_list,
             int32_t *__restrict__ long_list, Derive out) {
+    grid_dep_wait();
+    grid_dep_allow();
     const int n_int = __ldg(d_counts + 1);
     const int i = blockIdx.x * kThreads + threadIdx.x;
     if (i >= n_int) return;
@@ -364,6 +376,8 @@ k_sort_lists(const int32_t *__restrict__ tmp_p, const int32_t *__restrict__ star
              const int32_t *__restrict__ lengths, const int32_t *__restrict__ icell,
              const int32_t *__restrict__ lists, const int32_t *__restrict__ mid_list,
              const int32_t *__restrict__ long_list, const int32_t *__restrict__ cell_ids, int64_t nf, Derive out) {
+    grid_dep_wait();
+    grid_dep_allow();
     __shared__ int buf[kCtaSortMax];
     __shared__ int scratch[kWarps + 1];
     const int n_mid = __ldg(lists + 0), n_long = __ldg(lists + 1);
@@ -403,27 +417,41 @@ cudaError_t launch_build_map_counting(const BuildMapArgs &a) {
     int64_t zgrid = div_up(a.n_cells, kThreads * 4);
     if (zgrid > info.sm_count * 8) zgrid = info.sm_count * 8;
     if (zgrid < 1) zgrid = 1;
-    k_zero<<<static_cast<int>(zgrid), kThreads, 0, st>>>(ws.count, a.n_cells, ws.invalid, ws.lists);
+    // every kernel may launch while its predecessor drains (programmatic dependent launch)
+    cudaError_t e = launch_dependent(k_zero, dim3(static_cast<unsigned>(zgrid)), dim3(kThreads), 0, st, ws.count,
+                                     a.n_cells, ws.invalid, ws.lists);
     count_launch();
-    k_count_cells<<<nt, kThreads, 0, st>>>(a.cell_ids, nf, a.n_cells, vec, ws.count, ws.invalid);
+    if (e == cudaSuccess)
+        e = launch_dependent(k_count_cells, dim3(nt), dim3(kThreads), 0, st, a.cell_ids, nf, a.n_cells, vec, ws.count,
+                             ws.invalid);
     count_launch();
-    k_tile_sums<<<nct, kThreads, 0, st>>>(ws.count, a.n_cells, ws.tile_cnt, ws.tile_nz);
+    if (e == cudaSuccess)
+        e = launch_dependent(k_tile_sums, dim3(nct), dim3(kThreads), 0, st, ws.count, a.n_cells, ws.tile_cnt,
+                             ws.tile_nz);
     count_launch();
-    k_offsets<<<nct, kThreads, 0, st>>>(ws.count, a.n_cells, ws.tile_cnt, ws.tile_nz, ws.offset, a.interval_starts,
-                                        a.interval_lengths, ws.icell, ws.invalid, a.d_counts);
+    if (e == cudaSuccess)
+        e = launch_dependent(k_offsets, dim3(nct), dim3(kThreads), 0, st, ws.count, a.n_cells, ws.tile_cnt,
+                             ws.tile_nz, ws.offset, a.interval_starts, a.interval_lengths, ws.icell, ws.invalid,
+                             a.d_counts);
     count_launch();
-    k_scatter<<<nt, kThreads, 0, st>>>(a.cell_ids, nf, a.n_cells, vec, ws.offset, ws.tmp_p);
+    if (e == cudaSuccess)
+        e = launch_dependent(k_scatter, dim3(nt), dim3(kThreads), 0, st, a.cell_ids, nf, a.n_cells, vec, ws.offset,
+                             ws.tmp_p);
     count_launch();
     const int64_t max_int = nf < a.n_cells ? nf : a.n_cells;
     Derive out{a.ranks_depth, a.ranks_feat, a.ranks_bev, FastDiv(static_cast<uint32_t>(a.D) * a.H * a.W),
                FastDiv(static_cast<uint32_t>(a.H) * a.W)};
-    k_sort_runs<<<static_cast<int>(div_up(max_int, kThreads)), kThreads, 0, st>>>(
-        ws.tmp_p, a.interval_starts, a.interval_lengths, ws.icell, a.d_counts, ws.lists, ws.mid_list, ws.long_list,
-        out);
+    if (e == cudaSuccess)
+        e = launch_dependent(k_sort_runs, dim3(static_cast<unsigned>(div_up(max_int, kThreads))), dim3(kThreads), 0,
+                             st, ws.tmp_p, a.interval_starts, a.interval_lengths, ws.icell, a.d_counts, ws.lists,
+                             ws.mid_list, ws.long_list, out);
     count_launch();
-    k_sort_lists<<<info.sm_count * 4, kThreads, 0, st>>>(ws.tmp_p, a.interval_starts, a.interval_lengths, ws.icell,
-                                                        ws.lists, ws.mid_list, ws.long_list, a.cell_ids, nf, out);
+    if (e == cudaSuccess)
+        e = launch_dependent(k_sort_lists, dim3(info.sm_count * 4), dim3(kThreads), 0, st, ws.tmp_p,
+                             a.interval_starts, a.interval_lengths, ws.icell, ws.lists, ws.mid_list, ws.long_list,
+                             a.cell_ids, nf, out);
     count_launch();
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

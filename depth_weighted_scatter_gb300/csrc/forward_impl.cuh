@@ -631,6 +631,8 @@ __device__ __forceinline__ void fill_cta(const FwdParams &p, int fidx, FillSmem 
 
 template <int DT, int C, int OT>
 __global__ void __launch_bounds__(kThreads, BEVPOOL_FWD_MIN_CTAS) k_forward(const FwdParams p) {
+    grid_dep_wait();                               // the map build may still be draining (dependent launch)
+    grid_dep_allow();
     __shared__ __align__(16) FwdSmem<DT, C> sm;
     const int b = blockIdx.x;
     // compute CTAs (the long ones) first, then fill CTAs in the slots they free
@@ -681,9 +683,9 @@ cudaError_t launch_forward_t(const ForwardArgs &a) {
     p.n_fill = static_cast<int>(div_up(a.n_cells, fill_cells));
     p.out = static_cast<unsigned char *>(a.out);
     const int grid = p.n_compute + p.n_fill;
-    k_forward<DT, C, OT><<<grid, kThreads, 0, a.stream>>>(p);
+    const cudaError_t e = launch_dependent(k_forward<DT, C, OT>, dim3(grid), dim3(kThreads), 0, a.stream, p);
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace bevpool
