@@ -66,7 +66,7 @@
 #endif
 #ifndef BEVPOOL_FWD_DEPTH_SHFL
 #define BEVPOOL_FWD_DEPTH_SHFL 2          // who loads a point's depth: 0 every lane of the owner, 1 the lane
-#endif                                    // that fetched its ranks (a shuffle hands it out), 2 that for FP8 rows
+#endif                                    // that fetched its ranks (a shuffle hands it out), 2 see kDepthShfl
 // Compute CTAs per SM (one wave of them): with the output resident in L2,
 // two, leaving a slot for fill CTAs to run alongside; when the output streams
 // to DRAM, three (the gathers need the issue slots more than the fills).
@@ -88,9 +88,10 @@ constexpr int kFillCellsMin = 256;    // cells per fill CTA: a power of two in [
 constexpr int kFillCellsMax = 1024;
 
 // Whether the owner's fetch lane loads each point's depth (one load per point,
-// one shuffle per lane) instead of every lane loading it.
-template <int DT>
-constexpr bool kDepthShfl = BEVPOOL_FWD_DEPTH_SHFL == 1 || (BEVPOOL_FWD_DEPTH_SHFL == 2 && DT != 0);
+// one shuffle per lane) instead of every lane loading it: measured faster for
+// FP8 rows and for fp16 rows that take a whole warp (C = 256), slower else.
+template <int DT, int LPO>
+constexpr bool kDepthShfl = BEVPOOL_FWD_DEPTH_SHFL == 1 || (BEVPOOL_FWD_DEPTH_SHFL == 2 && (DT != 0 || LPO == 32));
 
 template <int DT, int C>
 struct FwdShape {
@@ -482,7 +483,7 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
             const unsigned ends = __ballot_sync(gmask, is_end) >> lane0;
             unsigned short d[S::BATCH];
             RawVec<S::VB> f[S::BATCH];
-            if constexpr (kDepthShfl<DT>) {
+            if constexpr (kDepthShfl<DT, S::LPO>) {
                 // lane kk loads the depth of point kk; shuffles hand depth and row to the owner's lanes
                 const int dv = rd >= 0 ? static_cast<int>(load_depth_h<DT>(p.depth, rd)) : 0;
                 int b[S::BATCH];
