@@ -1,10 +1,11 @@
 """Benchmark of the BEV-pooling hot path on one GB300 (or N independent replicas).
 
 A step is one pass of the whole hot path over one synthetic frame:
-bevpool_build_map (compaction, stable radix sort, index derivation,
-intervals) followed by bevpool_forward (interval-owned scatter-reduce).  L2 is
-flushed (a 256 MiB buffer is written) before the map build and again before
-the forward, so both run from HBM; each is bracketed by CUDA events on the
+bevpool_build_map (compaction and a counting sort by cell with the frustum
+order restored inside each run, index derivation, intervals) followed by
+bevpool_forward (interval-owned scatter-reduce).  L2 is flushed (a 256 MiB
+buffer is written) before the map build and again before the forward, so
+both run from HBM; each is bracketed by CUDA events on the
 stream it is launched on.  The headline value is the forward's device time in
 microseconds per call (lower is better); the map build and the whole step are
 reported beside it.

@@ -8,8 +8,9 @@
 // in FP32, rounded once to fp16, and writes every other cell as zeros, so
 // each output row is written exactly once and no atomics are used.
 //
-// One launch, two kinds of CTA (interleaved in blockIdx so both run from the
-// first wave):
+// One launch, two kinds of CTA: compute CTAs take the first block indices (one
+// resident wave of them, the long ones), fill CTAs the rest and run in the
+// slots the compute CTAs leave or free:
 //
 //   compute CTA  owns a chunk of consecutive intervals, i.e. a contiguous
 //                range of the sorted point arrays.  An owner is the LPO lanes

@@ -30,8 +30,10 @@
  *   - Layouts (frustum point index p = ((nc*D + d)*H + h)*W + w):
  *       cell_ids [NC*D*H*W] int32, -1 = point dropped, else in [0, n_cells)
  *       depth    [NC, D, H, W]  (element p belongs to frustum point p)
- *       feat     [NC, H, W, C]  (row r = (nc*H + h)*W + w holds C channels)
- *       out      [n_cells, C]   fp16 (IEEE binary16), row-major
+ *       feat     [NC, H, W, C]  (row r = (nc*H + h)*W + w holds C channels;
+ *                                NVFP4 rows: see bevpool_forward_nvfp4)
+ *       out      [n_cells, C]   fp16 (IEEE binary16), row-major (E4M3 codes
+ *                                from the calls with an E4M3 output)
  *   - Sizes: NC*D*H*W < 2^31, n_cells*C < 2^31.
  *   - Calls on different streams may run concurrently only if they share no
  *     output or workspace buffer.
