@@ -65,6 +65,12 @@
 #ifndef BEVPOOL_FWD_NVFP4_BATCH
 #define BEVPOOL_FWD_NVFP4_BATCH 6         // NVFP4 rows (one 16-element block a lane)
 #endif
+#ifndef BEVPOOL_FWD_LEAN_BATCH
+#define BEVPOOL_FWD_LEAN_BATCH 6          // fp16 rows, output streaming to DRAM: points in flight per owner
+#endif
+#ifndef BEVPOOL_FWD_LEAN_MIN_CTAS
+#define BEVPOOL_FWD_LEAN_MIN_CTAS 4       // ... with four CTAs per SM (64 registers), all computing
+#endif
 #ifndef BEVPOOL_FWD_DEPTH_SHFL
 #define BEVPOOL_FWD_DEPTH_SHFL 2          // who loads a point's depth: 0 every lane of the owner, 1 the lane
 #endif                                    // that fetched its ranks (a shuffle hands it out), 2 see kDepthShfl
@@ -94,7 +100,10 @@ constexpr int kFillCellsMax = 1024;
 template <int DT, int LPO>
 constexpr bool kDepthShfl = BEVPOOL_FWD_DEPTH_SHFL == 1 || (BEVPOOL_FWD_DEPTH_SHFL == 2 && (DT != 0 || LPO == 32));
 
-template <int DT, int C>
+// LEAN: the fp16 variant for outputs that stream to DRAM: fewer points in
+// flight per owner (BEVPOOL_FWD_LEAN_BATCH) so that 64 registers suffice and
+// four CTAs fit on an SM (more warps to hide the DRAM-bound stores).
+template <int DT, int C, bool LEAN = false>
 struct FwdShape {
     static constexpr bool NV = DT == kDtypeNVFP4;
     static constexpr int EB = DT == kDtypeF16 ? 2 : 1;          // input bytes per element (E4M3)
@@ -110,6 +119,7 @@ struct FwdShape {
     static constexpr int OWNERS = kWarps * OPW;                 // owners per CTA
     static constexpr int BATCH_CFG = NV                                  ? BEVPOOL_FWD_NVFP4_BATCH
                                      : VB >= 32                          ? BEVPOOL_FWD_BATCH32
+                                     : (DT == kDtypeF16 && LEAN)         ? BEVPOOL_FWD_LEAN_BATCH
                                      : (DT == kDtypeF16 || VB < 16)      ? BEVPOOL_FWD_BATCH
                                                                          : BEVPOOL_FWD_E4M3_BATCH16;
     static constexpr int BATCH = BATCH_CFG < LPO ? BATCH_CFG : LPO;   // points in flight per owner (<= LPO)
@@ -318,9 +328,9 @@ __device__ __forceinline__ void store_row_part(unsigned char *dst, const float *
 
 // ---------------------------------------------------------------- compute CTA
 
-template <int DT, int C>
+template <int DT, int C, bool LEAN = false>
 struct ComputeSmem {
-    using S = FwdShape<DT, C>;
+    using S = FwdShape<DT, C, LEAN>;
     int state[S::OWNERS];                         // how an owner's share starts (kHead / kCont / kPass)
     __align__(16) float slot[2][S::OWNERS][C];    // partial rows of intervals cut by a share boundary
 };
@@ -334,9 +344,9 @@ struct FillSmem {
     unsigned mark[kFillCellsMax / 32];
 };
 
-template <int DT, int C>
+template <int DT, int C, bool LEAN = false>
 union FwdSmem {
-    ComputeSmem<DT, C> c;
+    ComputeSmem<DT, C, LEAN> c;
     FillSmem f;
 };
 
@@ -401,9 +411,9 @@ __device__ __forceinline__ void cta_next_starts(const FwdParams &p, int n, int n
     *t1 = min(max(r1, *t0), n);
 }
 
-template <int DT, int C, int OT>
-__device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, ComputeSmem<DT, C> &sm) {
-    using S = FwdShape<DT, C>;
+template <int DT, int C, int OT, bool LEAN>
+__device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, ComputeSmem<DT, C, LEAN> &sm) {
+    using S = FwdShape<DT, C, LEAN>;
     constexpr int OB = OT == kOutF16 ? 2 : 1;      // output bytes per element
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
@@ -631,24 +641,25 @@ __device__ __forceinline__ void fill_cta(const FwdParams &p, int fidx, FillSmem 
 
 // ---------------------------------------------------------------- kernel
 
-template <int DT, int C, int OT>
-__global__ void __launch_bounds__(kThreads, BEVPOOL_FWD_MIN_CTAS) k_forward(const FwdParams p) {
+template <int DT, int C, int OT, bool LEAN>
+__global__ void __launch_bounds__(kThreads, LEAN ? BEVPOOL_FWD_LEAN_MIN_CTAS : BEVPOOL_FWD_MIN_CTAS)
+    k_forward(const FwdParams p) {
     grid_dep_wait();                               // the map build may still be draining (dependent launch)
     grid_dep_allow();
-    __shared__ __align__(16) FwdSmem<DT, C> sm;
+    __shared__ __align__(16) FwdSmem<DT, C, LEAN> sm;
     const int b = blockIdx.x;
     // compute CTAs (the long ones) first, then fill CTAs in the slots they free
     const bool compute = b < p.n_compute;
     const int idx = compute ? b : b - p.n_compute;
     if (compute)
-        compute_cta<DT, C, OT>(p, idx, sm.c);
+        compute_cta<DT, C, OT, LEAN>(p, idx, sm.c);
     else
         fill_cta<DT, C, OT>(p, idx, sm.f);
 }
 
-template <int DT, int C, int OT>
-cudaError_t launch_forward_t(const ForwardArgs &a) {
-    using S = FwdShape<DT, C>;
+template <int DT, int C, int OT, bool LEAN>
+cudaError_t launch_forward_v(const ForwardArgs &a) {
+    using S = FwdShape<DT, C, LEAN>;
     FwdParams p;
     p.depth = a.depth;
     p.feat = a.feat;
@@ -670,7 +681,8 @@ cudaError_t launch_forward_t(const ForwardArgs &a) {
     // points per owner; the points per CTA are set on the device from the
     // actual count.
     const int64_t slots = static_cast<int64_t>(a.sm_count > 0 ? a.sm_count : 148) *
-                          (a.streaming_stores ? BEVPOOL_FWD_CTAS_PER_SM_DRAM : BEVPOOL_FWD_CTAS_PER_SM_L2);
+                          (LEAN ? BEVPOOL_FWD_LEAN_MIN_CTAS
+                           : (a.streaming_stores ? BEVPOOL_FWD_CTAS_PER_SM_DRAM : BEVPOOL_FWD_CTAS_PER_SM_L2));
     int64_t n_compute = div_up(a.n_points, static_cast<int64_t>(S::OWNERS) * S::BATCH);
     if (n_compute > slots) n_compute = slots;
     if (n_compute < 1) n_compute = 1;
@@ -685,9 +697,19 @@ cudaError_t launch_forward_t(const ForwardArgs &a) {
     p.n_fill = static_cast<int>(div_up(a.n_cells, fill_cells));
     p.out = static_cast<unsigned char *>(a.out);
     const int grid = p.n_compute + p.n_fill;
-    const cudaError_t e = launch_dependent(k_forward<DT, C, OT>, dim3(grid), dim3(kThreads), 0, a.stream, p);
+    const cudaError_t e = launch_dependent(k_forward<DT, C, OT, LEAN>, dim3(grid), dim3(kThreads), 0, a.stream, p);
     count_launch();
     return e;
+}
+
+// fp16 rows whose output streams to DRAM take the lean variant (measured: DRAM
+// batch 122.9 -> 114.7 us; with the output in L2 it was not faster).
+template <int DT, int C, int OT>
+cudaError_t launch_forward_t(const ForwardArgs &a) {
+    if constexpr (DT == kDtypeF16) {
+        if (a.streaming_stores) return launch_forward_v<DT, C, OT, true>(a);
+    }
+    return launch_forward_v<DT, C, OT, false>(a);
 }
 
 }  // namespace bevpool

@@ -238,3 +238,28 @@ def test_forward_rejects_bad_arguments(bp, wl_cache):
     with pytest.raises(bp.BevpoolError) as ei:
         bp.forward(m, depth, feat, wl.C, out=out[1:])     # misaligned output
     assert ei.value.status == bp.BEVPOOL_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("C", [8, 80, 256])
+def test_streaming_regime_channel_counts(bp, C):
+    """A grid big enough that the output streams past L2 selects the kernels
+    for that regime (evict-first stores; for fp16 the variant with four CTAs
+    per SM): parity on every row, the few occupied ones and the many zeros."""
+    from depth_weighted_scatter_gb300 import workloads
+
+    cells = (72 << 20) // (2 * C) + 1                   # > 72 MiB of fp16 output
+    NC, D, H, W = 2, 11, 9, 13
+    rng = np.random.default_rng(C + 77)
+    nf = NC * D * H * W
+    cid = rng.integers(0, cells, nf).astype(np.int32)
+    hot = rng.random(nf) < 0.3
+    cid[hot] = rng.integers(0, 50, int(hot.sum()))      # a dense corner with long intervals
+    cid[rng.random(nf) < 0.2] = -1
+    wl = workloads.custom(NC, D, H, W, C, cells, cid, seed=C, name=f"stream_C{C}")
+    c_d, depth, feat = upload(wl)
+    m = _gpu_map(bp, wl, c_d)
+    _check_map(bp, wl, m)
+    out = torch.full((cells, C), float("nan"), dtype=torch.float16, device="cuda")
+    gpu_forward(wl, m, depth, feat, out=out)
+    torch.cuda.synchronize()
+    assert_forward_close(wl, out, oracle_forward(wl))
