@@ -13,6 +13,9 @@ reported beside it.
 Also reported, on one line of JSON:
   roofline      the forward kernel's algorithmic bytes / event time against
                 the measured HBM copy bandwidth;
+  roofline_l2   (working set within half the L2) the gather-level bytes of
+                one forward / its warm-L2 CUDA-graph time, against the L2
+                copy bandwidth measured in the same run (bevpool_probe_l2);
   e2e           the same forward driven from pinned host buffers through the
                 C ABI (H2D of depth+feat, forward, D2H of the output);
   cpu_baseline  the FP64 oracle (single thread) on the same workload;
@@ -46,10 +49,17 @@ FORWARD_SOURCES = ["forward_impl.cuh", "forward_f16.cu", "forward_e4m3.cu", "for
 
 
 def forward_source_hash() -> str:
+    """Hash of the forward's code (comments stripped, so editing a comment
+    keeps the ncu records that were taken on the same code)."""
+    import re
+
     h = hashlib.sha1()
     for f in FORWARD_SOURCES:
-        with open(os.path.join(ROOT, "depth_weighted_scatter_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "depth_weighted_scatter_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(line.rstrip() for line in text.splitlines() if line.strip()).encode())
     return h.hexdigest()[:16]
 
 
@@ -92,6 +102,33 @@ def bytes_model(wl, n_points: int, n_intervals: int, out_bytes: int = 2) -> dict
     footprint = idx + iv + depth + feat + out
     gather = idx + iv + n_points * eb + n_points * row + out
     return dict(index=idx, intervals=iv, depth=depth, feat=feat, out=out, footprint=footprint, gather=gather)
+
+
+def l2_probe(device, stream, mib: int = 64, passes: int = 16, reps: int = 5) -> dict:
+    """L2 bandwidth of a buffer resident in L2 (bevpool_probe_l2): read, write
+    and copy of `mib` MiB, `passes` passes per launch, best of `reps` launches,
+    GB/s.  Copy counts the bytes read plus the bytes written (a STREAM copy,
+    the convention of the HBM peak)."""
+    import torch
+
+    from depth_weighted_scatter_gb300 import bevpool
+
+    buf = torch.ones(mib << 18, dtype=torch.int32, device=device)
+    sink = torch.zeros(1, dtype=torch.int32, device=device)
+    nbytes = buf.numel() * 4
+    out = {"buffer_mib": mib, "passes": passes, "launches": reps}
+    for name, mode in (("read", bevpool.PROBE_READ), ("write", bevpool.PROBE_WRITE), ("copy", bevpool.PROBE_COPY)):
+        bevpool.probe_l2(buf, 2, mode=mode, sink=sink, stream=stream)      # brings the buffer into L2
+        best = float("inf")
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            bevpool.probe_l2(buf, passes, mode=mode, sink=sink, stream=stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b) * 1e-3)
+        out[f"{name}_gbs"] = passes * nbytes / best / 1e9
+    return out
 
 
 class ClockSampler:
@@ -404,6 +441,21 @@ def run_ours(args) -> None:
         except Exception as e:
             frame_us = f"unavailable: {type(e).__name__}"
 
+    # L2 roofline (working set resident in L2): the gather-level bytes of one
+    # forward over the warm-L2 graph time, against the L2 copy bandwidth the
+    # probe measures on this GPU in this run.
+    roof_l2 = None
+    l2_bytes = torch.cuda.get_device_properties(device).L2_cache_size
+    bm0 = bytes_model(wl, n_pts, n_int, 1 if e4m3_out else 2)
+    if bm0["footprint"] <= l2_bytes // 2 and isinstance(warm_us, float):
+        probe = l2_probe(device, stream)
+        achieved_l2 = bm0["gather"] / (warm_us * 1e-6) / 1e9
+        roof_l2 = {"bound": "l2", "achieved": achieved_l2, "peak": probe["copy_gbs"], "unit": "GB/s",
+                   "frac": achieved_l2 / probe["copy_gbs"], "bytes_per_launch": bm0["gather"],
+                   "time_us": warm_us, "time": "warm-L2 CUDA-graph median per call",
+                   "peak_source": "bevpool_probe_l2 copy (read + write bytes), 64 MiB resident, best of 5",
+                   "probe": probe}
+
     # End to end through the C ABI from pinned host buffers.
     out_h = torch.empty((wl.n_cells, wl.C), dtype=out.dtype).pin_memory()
     e2e_steps = min(args.steps, 200)
@@ -453,6 +505,7 @@ def run_ours(args) -> None:
                      "frac": achieved / peak, "traffic": recorded_traffic(traffic_key),
                      "kernel": "k_forward", "bytes_per_launch": bm["footprint"],
                      "peak_source": f"hbm_gbs of MEASURED_PEAKS.json ({peak_kind})"},
+        "roofline_l2": roof_l2,
         "cpu_baseline": (cpu_oracle_time(wl, out_scale=out_scale)
                          if (world == 1 and not args.no_cpu_baseline) else None),
         "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -70,6 +70,8 @@ _lib.bevpool_pool_frame.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, ctypes.c_
 _lib.bevpool_pool_frame.restype = ctypes.c_int
 _lib.bevpool_validate_map.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]
 _lib.bevpool_validate_map.restype = ctypes.c_int
+_lib.bevpool_probe_l2.argtypes = [_i32, _vp, _sz, _i32, _vp, _vp]
+_lib.bevpool_probe_l2.restype = ctypes.c_int
 
 
 class BevpoolError(RuntimeError):
@@ -165,6 +167,10 @@ def bevpool_validate_map(ranks_depth: int, ranks_feat: int, ranks_bev: int, inte
     return _lib.bevpool_validate_map(ranks_depth, ranks_feat, ranks_bev, interval_starts, interval_lengths,
                                      n_points, n_intervals, NC, D, H, W, n_cells, d_result, _host_ptr(h_result),
                                      stream)
+
+
+def bevpool_probe_l2(mode: int, buf: int, nbytes: int, passes: int, d_sink: int, stream: int) -> int:
+    return _lib.bevpool_probe_l2(mode, buf, nbytes, passes, d_sink, stream)
 
 
 # ---------------------------------------------------------------- tensor helpers (torch = memory + streams)
@@ -325,3 +331,18 @@ def pool_frame(cell_ids, depth, feat, NC: int, D: int, H: int, W: int, n_cells: 
         raise BevpoolError(st, "bevpool_pool_frame")
     m.n_points = m.n_intervals = None
     return out, m
+
+
+PROBE_READ, PROBE_WRITE, PROBE_COPY = 0, 1, 2
+
+
+def probe_l2(buf, passes: int, *, mode: int = PROBE_READ, sink=None, stream=None):
+    """One launch of the L2 streaming probe over the bytes of ``buf`` (a
+    contiguous device tensor); see bevpool_probe_l2.  The read probe adds the
+    word sum of every pass to ``sink`` (a device tensor of one 32-bit element
+    the caller zeroed; the sum wraps mod 2^32)."""
+    nbytes = buf.numel() * buf.element_size()
+    st = bevpool_probe_l2(mode, buf.data_ptr(), nbytes, passes, sink.data_ptr() if sink is not None else 0,
+                          _stream(stream))
+    if st != BEVPOOL_OK:
+        raise BevpoolError(st, "bevpool_probe_l2")

@@ -266,6 +266,10 @@ bevpool_status forward_impl(bevpool_dtype dtype, const void *depth, const void *
     const int64_t footprint = static_cast<int64_t>(n_points) * 12 + static_cast<int64_t>(n_intervals) * 8 +
                               nf * eb + feat_bytes + static_cast<int64_t>(n_cells) * C * ob;
     a.streaming_stores = footprint > static_cast<int64_t>(info.l2_bytes) / 2 ? 1 : 0;
+    // Device counts bounded by the whole frustum (what bevpool_pool_frame
+    // passes) say nothing about the actual count: size the launch for one
+    // resident wave and leave the choice of variant to the memory regime.
+    a.loose_capacity = d_counts && n_points >= nf ? 1 : 0;
     a.sm_count = info.sm_count;
     a.out = out;
     a.stream = static_cast<cudaStream_t>(stream);

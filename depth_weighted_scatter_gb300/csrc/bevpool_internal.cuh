@@ -158,6 +158,7 @@ struct ForwardArgs {
     float scale;              // depth_scale * feat_scale (/ out_scale for an E4M3 output)
     int out_e4m3;             // 1: E4M3 output codes, 0: fp16 output
     int streaming_stores;     // 1: evict-first output stores (HBM regime)
+    int loose_capacity;       // 1: n_points is the whole frustum, not a bound close to the device count
     int sm_count;             // SMs of the current device (launch sizing)
     void *out;
     cudaStream_t stream;

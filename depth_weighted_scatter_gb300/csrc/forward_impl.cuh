@@ -8,24 +8,27 @@
 // in FP32, rounded once to fp16, and writes every other cell as zeros, so
 // each output row is written exactly once and no atomics are used.
 //
-// One launch, two kinds of CTA: compute CTAs take the first block indices (one
-// resident wave of them, the long ones), fill CTAs the rest and run in the
-// slots the compute CTAs leave or free:
+// One launch, two kinds of CTA: compute CTAs take the first block indices (the
+// long ones), fill CTAs the rest and run in the slots the compute CTAs leave
+// or free:
 //
 //   compute CTA  owns a chunk of consecutive intervals, i.e. a contiguous
-//                range of the sorted point arrays.  An owner is the LPO lanes
-//                that together hold one C-channel row (VB bytes per lane).
-//                Owners take equal shares of the chunk's points and walk them
-//                in lockstep, BATCH points at a time: each lane fetches one
-//                point's ranks, warp shuffles broadcast them, and each owner
-//                then has BATCH depth loads and feature-row gathers in flight
-//                ("depth loaded once per scatter point").  An interval ends
-//                where ranks_bev changes, so the ends of a batch are one
-//                bit mask, known before its FMAs; at an end the owner rounds
-//                its FP32 row to fp16 and stores it.  An interval cut by a
-//                share boundary leaves FP32 partial rows in shared memory;
-//                after a barrier the owner that started it adds them in owner
-//                order, so the sum order is fixed and the result deterministic.
+//                range of the sorted point arrays with about the same number
+//                of points as every other compute CTA.  It works in rounds:
+//                the whole CTA first stages the round's points in shared
+//                memory (coalesced loads of the three rank arrays, the depth
+//                gather "once per scatter point", and one 16-byte record per
+//                point with the feature row, the depth value and an
+//                interval-end bit from the change of ranks_bev), then the
+//                owners walk the records.  An owner is the LPO lanes that
+//                together hold one C-channel row (VB bytes per lane); owners
+//                take equal shares of the round and walk them independently,
+//                BATCH rows in flight each.  At an interval end the owner
+//                rounds its FP32 row to the output type and stores it.  An
+//                interval cut by a share boundary leaves FP32 partial rows in
+//                shared memory; after a barrier the owner that started it
+//                adds them in owner order, so the sum order is fixed and the
+//                result deterministic.
 //
 //   fill CTA     owns a tile of 256-1024 consecutive cells.  It finds the
 //                tile's points in the sorted ranks_bev with a CTA-wide k-ary
@@ -36,6 +39,7 @@
 #pragma once
 
 #include <climits>
+#include <type_traits>
 
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -71,9 +75,21 @@
 #ifndef BEVPOOL_FWD_LEAN_MIN_CTAS
 #define BEVPOOL_FWD_LEAN_MIN_CTAS 4       // ... with four CTAs per SM (64 registers), all computing
 #endif
-#ifndef BEVPOOL_FWD_DEPTH_SHFL
-#define BEVPOOL_FWD_DEPTH_SHFL 2          // who loads a point's depth: 0 every lane of the owner, 1 the lane
-#endif                                    // that fetched its ranks (a shuffle hands it out), 2 see kDepthShfl
+#ifndef BEVPOOL_FWD_PIPELINE
+#define BEVPOOL_FWD_PIPELINE 0            // > 0: fp16 owners walk in a two-stage pipeline of this many points
+#endif
+#ifndef BEVPOOL_FWD_PIPELINE_FP8
+#define BEVPOOL_FWD_PIPELINE_FP8 2        // the same for E4M3 rows
+#endif
+#ifndef BEVPOOL_FWD_PIPELINE_NVFP4
+#define BEVPOOL_FWD_PIPELINE_NVFP4 2      // the same for NVFP4 rows
+#endif
+#ifndef BEVPOOL_FWD_MULTIWAVE
+#define BEVPOOL_FWD_MULTIWAVE 64          // > 0: compute CTAs of at most a round less this many points each
+#endif
+#ifndef BEVPOOL_FWD_LEAN_WORK_PER_SM
+#define BEVPOOL_FWD_LEAN_WORK_PER_SM 131072   // fp16 rows with at least this many point-channels per SM run lean
+#endif
 // Compute CTAs per SM (one wave of them): with the output resident in L2,
 // two, leaving a slot for fill CTAs to run alongside; when the output streams
 // to DRAM, three (the gathers need the issue slots more than the fills).
@@ -93,12 +109,6 @@ constexpr int kOutF16 = 0;     // output element: fp16 (round to nearest even)
 constexpr int kOutE4M3 = 1;    // output element: OCP E4M3 code (round to nearest even, saturating)
 constexpr int kFillCellsMin = 256;    // cells per fill CTA: a power of two in [min, max], chosen per call
 constexpr int kFillCellsMax = 1024;
-
-// Whether the owner's fetch lane loads each point's depth (one load per point,
-// one shuffle per lane) instead of every lane loading it: measured faster for
-// FP8 rows and for fp16 rows that take a whole warp (C = 256), slower else.
-template <int DT, int LPO>
-constexpr bool kDepthShfl = BEVPOOL_FWD_DEPTH_SHFL == 1 || (BEVPOOL_FWD_DEPTH_SHFL == 2 && (DT != 0 || LPO == 32));
 
 // LEAN: the fp16 variant for outputs that stream to DRAM: fewer points in
 // flight per owner (BEVPOOL_FWD_LEAN_BATCH) so that 64 registers suffice and
@@ -122,7 +132,7 @@ struct FwdShape {
                                      : (DT == kDtypeF16 && LEAN)         ? BEVPOOL_FWD_LEAN_BATCH
                                      : (DT == kDtypeF16 || VB < 16)      ? BEVPOOL_FWD_BATCH
                                                                          : BEVPOOL_FWD_E4M3_BATCH16;
-    static constexpr int BATCH = BATCH_CFG < LPO ? BATCH_CFG : LPO;   // points in flight per owner (<= LPO)
+    static constexpr int BATCH = BATCH_CFG;                       // points in flight per owner
     static_assert(ROWB % VB == 0 && (VB == 2 || VB == 4 || VB == 8 || VB == 16 || VB == 32), "bad vector width");
     static_assert(LPO >= 4 && LPO <= 32, "bad lane mapping");
     static_assert(C % 8 == 0 && (!NV || C % 16 == 0), "C must be a multiple of 8 (16 for NVFP4)");
@@ -289,8 +299,13 @@ __device__ __forceinline__ void store_row_part(unsigned char *dst, const float *
     if constexpr (OT == kOutF16) {
         constexpr int NW = EPL / 2;   // 32-bit words
         uint32_t w[NW];
+        if (scale == 1.f) {                        // x * 1 == x: skip the multiplies (the usual fp16 case)
 #pragma unroll
-        for (int i = 0; i < NW; ++i) w[i] = pack_half2(acc[2 * i] * scale, acc[2 * i + 1] * scale);
+            for (int i = 0; i < NW; ++i) w[i] = pack_half2(acc[2 * i], acc[2 * i + 1]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < NW; ++i) w[i] = pack_half2(acc[2 * i] * scale, acc[2 * i + 1] * scale);
+        }
         if constexpr (NW % 4 == 0) {
 #pragma unroll
             for (int q = 0; q < NW / 4; ++q)
@@ -328,17 +343,41 @@ __device__ __forceinline__ void store_row_part(unsigned char *dst, const float *
 
 // ---------------------------------------------------------------- compute CTA
 
+// One point of a compute CTA's chunk, staged in shared memory by the whole
+// CTA before the owners walk it (one 16-byte load per point and lane).
+struct __align__(16) PointRec {
+    int32_t row;        // feature row (ranks_feat); 0 for a skipped point
+    uint32_t dflags;    // depth value as fp16 bits | kEndBit | kSkipBit
+    int32_t bev;        // cell (ranks_bev)
+    int32_t pad;
+};
+constexpr uint32_t kEndBit = 1u << 16;    // the point is the last of its interval
+constexpr uint32_t kSkipBit = 1u << 17;   // a rank is out of range: the point adds nothing
+constexpr uint32_t kNoCellBit = 1u << 18; // the cell is out of range: its interval is not stored
+
 template <int DT, int C, bool LEAN = false>
 struct ComputeSmem {
     using S = FwdShape<DT, C, LEAN>;
-    int state[S::OWNERS];                         // how an owner's share starts (kHead / kCont / kPass)
-    __align__(16) float slot[2][S::OWNERS][C];    // partial rows of intervals cut by a share boundary
+    // partial rows: the slot of every owner, and the carry of an interval
+    // that runs on into the next round (two buffers, by round parity)
+    static constexpr int ROW_BYTES = (S::OWNERS + 2) * C * 4;
+    // points per round: as many 16-byte records as fit beside the rows in
+    // 46 KB of static shared memory, a multiple of the CTA size, at most 1024
+    static constexpr int ROUND_FIT = ((46 * 1024 - ROW_BYTES) / 16) / kThreads * kThreads;
+    static constexpr int ROUND = ROUND_FIT < 1024 ? ROUND_FIT : 1024;
+    static_assert(ROUND >= kThreads, "partial rows leave no room for point records");
+    PointRec rec[ROUND];
+    int state[S::OWNERS];                         // how an owner's share starts (kHead / kCont / kPass / kEmpty)
+    int carry_bev[2];
+    __align__(16) float slot[S::OWNERS][C];       // first partial row of a share that starts inside an interval
+    __align__(16) float carry[2][C];
 };
 
-// How an owner's share of the chunk starts:
-constexpr int kHead = 0;   // at the first point of an interval (or the share is empty)
-constexpr int kCont = 1;   // inside an interval that ends within the share: its partial is in slot[0]
-constexpr int kPass = 2;   // inside an interval that runs through the whole share: its partial is in slot[0]
+// How an owner's share of a round starts:
+constexpr int kHead = 0;    // at the first point of an interval
+constexpr int kCont = 1;    // inside an interval that ends within the share: its partial is in the slot
+constexpr int kPass = 2;    // inside an interval that runs through the whole share: its partial is in the slot
+constexpr int kEmpty = 3;   // the share is empty (the last owners of a short round)
 
 struct FillSmem {
     unsigned mark[kFillCellsMax / 32];
@@ -411,10 +450,19 @@ __device__ __forceinline__ void cta_next_starts(const FwdParams &p, int n, int n
     *t1 = min(max(r1, *t0), n);
 }
 
+// acc[0 .. EPL) of an interval: to the output row of cell bev (in range),
+// scaled and rounded.
+template <int OT, int C, int EPL>
+__device__ __forceinline__ void store_interval(const FwdParams &p, int bev, int ol, const float *acc) {
+    constexpr int OB = OT == kOutF16 ? 2 : 1;
+    store_row_part<OT, EPL>(p.out + (static_cast<int64_t>(bev) * C + ol * EPL) * OB, acc, p.scale, p.streaming);
+}
+
 template <int DT, int C, int OT, bool LEAN>
 __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, ComputeSmem<DT, C, LEAN> &sm) {
     using S = FwdShape<DT, C, LEAN>;
-    constexpr int OB = OT == kOutF16 ? 2 : 1;      // output bytes per element
+    using SM = ComputeSmem<DT, C, LEAN>;
+    constexpr int U = S::BATCH;                    // points in flight per owner
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
     __shared__ int s_bounds[2];
@@ -426,183 +474,309 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
     if (n_pts <= 0) return;                        // uniform over the CTA
 
     // 1. the CTA's points: [cidx * ppc, (cidx + 1) * ppc) with both ends moved
-    //    forward to interval starts, so no interval is split between CTAs and
-    //    every CTA gets about the same number of points.
+    //    forward to interval starts (T0, T1), so no interval is split between
+    //    CTAs and every CTA gets about the same number of points.  The
+    //    starts are found in the staged windows themselves; only a window
+    //    without any start (one long interval) falls back to a search.
     const int ppc = static_cast<int>(p.n_compute_div.div(static_cast<uint32_t>(n_pts - 1))) + 1;
-    const int64_t x0 = static_cast<int64_t>(cidx) * ppc;
-    if (x0 >= n_pts) return;
-    const int x1 = static_cast<int>(min(static_cast<int64_t>(n_pts), x0 + ppc));
-    int T0, T1;
-    cta_next_starts(p, n_pts, n_int, static_cast<int>(x0), x1, &T0, &T1, s_bounds);
-    if (T1 <= T0) return;                          // inside one long interval: the CTA before owns it
-    const int P = T1 - T0;
+    const int64_t x0l = static_cast<int64_t>(cidx) * ppc;
+    if (x0l >= n_pts) return;
+    const int x0 = static_cast<int>(x0l);
+    const int x1 = static_cast<int>(min(static_cast<int64_t>(n_pts), x0l + ppc));
+    __shared__ int s_min[2][kWarps];
 
-    // 2. owners take equal shares of the chunk's points and walk them in
-    //    lockstep (same trip count for every owner of a warp).  A share that
-    //    starts inside an interval leaves its first partial row in slot[0]; a
-    //    share that ends inside an interval it started leaves a partial in
-    //    slot[1] and adds the later owners' slot[0] rows after the barrier.
     const int og = lane / S::LPO;                  // owner within warp
     const int ol = lane % S::LPO;                  // lane within owner
     const bool active = og < S::OPW;
     const int o = active ? warp * S::OPW + og : 0;
-    const int lane0 = og * S::LPO;
-    const unsigned gmask = (S::LPO == 32 ? 0xffffffffu : ((1u << S::LPO) - 1u)) << lane0;
     const unsigned char *featp = static_cast<const unsigned char *>(p.feat) + ol * S::VB;
-    const int share = (P + S::OWNERS - 1) / S::OWNERS;
-    const int beg = active ? min(P, o * share) : P;
-    const int end = active ? min(P, beg + share) : P;
+    [[maybe_unused]] const unsigned char *blockp = p.feat_block + ol;   // NVFP4: the lane's block scale
 
-    bool head_cut = false;                         // this owner finishes an interval cut by its share end
-    int head_bev = -1;
-    if (active) {
-        const bool head = beg == 0 || beg >= end || __ldg(p.ranks_bev + T0 + beg - 1) != __ldg(p.ranks_bev + T0 + beg);
-        float acc[S::EPL];
+    int T0 = -1, T1 = -1;                          // known once found (uniform over the CTA)
+    int w0 = x0;                                   // first point of the staged window
+    bool round_head = true;                        // the round's first point starts an interval
+    for (int rnd = 0;; ++rnd) {
+        const int W = min(SM::ROUND, n_pts - w0);
+        const int cb = rnd & 1;                    // carry buffer read this round (the other is written)
+
+        // 2. stage the window [w0, w0 + W): every thread takes points tid,
+        //    tid + 256, ...; all rank loads first, then the depth gathers,
+        //    then the records.
+        constexpr int K = SM::ROUND / kThreads;
+        int cell[K], prv[K], nxt[K], rx[K], ry[K];
 #pragma unroll
-        for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
-        bool to_slot = !head;                      // the next finished segment continues a previous share
-        // lane ol < BATCH holds the ranks of point v0 + ol: depth / feature
-        // rows for points of the share (-1 otherwise), the cell for points of the chunk
-        auto fetch_idx = [&](int v0, int &ra, int &rb, int &rc) {
-            ra = -1;
-            rb = -1;
-            rc = -1;
-            const int j = v0 + ol;
-            if (ol < S::BATCH && j < P) {
-                rc = __ldg(p.ranks_bev + T0 + j);
-                if (j < end) {
-                    const int x = __ldg(p.ranks_depth + T0 + j);
-                    const int y = __ldg(p.ranks_feat + T0 + j);
-                    if (x >= 0 && x < p.n_depth && y >= 0 && y < p.n_feat_rows) {
-                        ra = x;
-                        rb = y;
-                    }
-                }
+        for (int k = 0; k < K; ++k) {
+            const int i = threadIdx.x + k * kThreads;
+            const int t = w0 + i;
+            cell[k] = prv[k] = nxt[k] = rx[k] = ry[k] = -1;
+            if (i < W) {
+                cell[k] = __ldg(p.ranks_bev + t);
+                if (t > 0) prv[k] = __ldg(p.ranks_bev + t - 1);
+                if (t + 1 < n_pts) nxt[k] = __ldg(p.ranks_bev + t + 1);
+                rx[k] = __ldg(p.ranks_depth + t);
+                ry[k] = __ldg(p.ranks_feat + t);
             }
-        };
-        int rd, rf, rc;
-        fetch_idx(beg, rd, rf, rc);
-        for (int v0 = beg; v0 < beg + share; v0 += S::BATCH) {
-            int rd_next, rf_next, rc_next;
-            fetch_idx(v0 + S::BATCH, rd_next, rf_next, rc_next);   // prefetch the next batch's ranks
-            // bit kk of ends: point v0 + kk is the last of its interval
-            const int succ_in = __shfl_sync(gmask, rc, lane0 + min(ol + 1, S::BATCH - 1));
-            const int succ_nx = __shfl_sync(gmask, rc_next, lane0);
-            const int j = v0 + ol;
-            const bool is_end = ol < S::BATCH && j < end &&
-                                (j + 1 == P || rc != (ol + 1 < S::BATCH ? succ_in : succ_nx));
-            const unsigned ends = __ballot_sync(gmask, is_end) >> lane0;
-            unsigned short d[S::BATCH];
-            RawVec<S::VB> f[S::BATCH];
-            if constexpr (kDepthShfl<DT, S::LPO>) {
-                // lane kk loads the depth of point kk; shuffles hand depth and row to the owner's lanes
-                const int dv = rd >= 0 ? static_cast<int>(load_depth_h<DT>(p.depth, rd)) : 0;
-                int b[S::BATCH];
+        }
+        bool skip_any = false;
+        int f0 = INT_MAX, f1 = INT_MAX;            // first interval start at or after x0 / x1
 #pragma unroll
-                for (int kk = 0; kk < S::BATCH; ++kk) b[kk] = __shfl_sync(gmask, rf, lane0 + kk);
-                [[maybe_unused]] unsigned short sh[S::BATCH];
-#pragma unroll
-                for (int kk = 0; kk < S::BATCH; ++kk) {
-                    if (b[kk] >= 0) {
-                        f[kk] = load_vec<S::VB>(featp + static_cast<int64_t>(b[kk]) * S::ROWB);
-                        if constexpr (S::NV) {
-                            const unsigned char sc =
-                                __ldg(p.feat_block + static_cast<int64_t>(b[kk]) * (C / 16) + ol);
-                            sh[kk] = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sc), __NV_E4M3).x;
-                        }
-                    } else {                                     // past the share, or an invalid rank: adds +0
-#pragma unroll
-                        for (int i = 0; i < RawVec<S::VB>::NW; ++i) f[kk].w[i] = 0u;
-                        if constexpr (S::NV) sh[kk] = 0;
-                    }
+        for (int k = 0; k < K; ++k) {
+            const int i = threadIdx.x + k * kThreads;
+            const int t = w0 + i;
+            if (i < W) {
+                const bool ok = rx[k] >= 0 && rx[k] < p.n_depth && ry[k] >= 0 && ry[k] < p.n_feat_rows;
+                const bool start = t == 0 || prv[k] != cell[k];
+                const bool end = t + 1 == n_pts || nxt[k] != cell[k];
+                if (start) {
+                    f0 = min(f0, t);
+                    if (t >= x1) f1 = min(f1, t);
                 }
-#pragma unroll
-                for (int kk = 0; kk < S::BATCH; ++kk) {
-                    d[kk] = static_cast<unsigned short>(__shfl_sync(gmask, dv, lane0 + kk));
-                    if constexpr (S::NV) d[kk] = mul_f16_bits(d[kk], sh[kk]);   // depth x block scale (exact in fp16)
-                }
-            } else {
-                int a[S::BATCH], b[S::BATCH];
-#pragma unroll
-                for (int kk = 0; kk < S::BATCH; ++kk) {
-                    a[kk] = __shfl_sync(gmask, rd, lane0 + kk);
-                    b[kk] = __shfl_sync(gmask, rf, lane0 + kk);
-                }
-#pragma unroll
-                for (int kk = 0; kk < S::BATCH; ++kk) {
-                    if (a[kk] >= 0) {
-                        d[kk] = load_depth_h<DT>(p.depth, a[kk]);
-                        f[kk] = load_vec<S::VB>(featp + static_cast<int64_t>(b[kk]) * S::ROWB);
-                        if constexpr (S::NV) {                   // depth x the lane's block scale (exact in fp16)
-                            const unsigned char sc =
-                                __ldg(p.feat_block + static_cast<int64_t>(b[kk]) * (C / 16) + ol);
-                            const __half_raw sh =
-                                __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sc), __NV_E4M3);
-                            d[kk] = mul_f16_bits(d[kk], sh.x);
-                        }
-                    } else {                                     // past the share, or an invalid rank: adds +0
-                        d[kk] = 0;
-#pragma unroll
-                        for (int i = 0; i < RawVec<S::VB>::NW; ++i) f[kk].w[i] = 0u;
-                    }
-                }
+                const uint32_t d = ok ? load_depth_h<DT>(p.depth, rx[k]) : 0u;
+                PointRec q;
+                q.row = ok ? ry[k] : 0;
+                q.dflags = d | (end ? kEndBit : 0u) | (ok ? 0u : kSkipBit) |
+                           ((cell[k] >= 0 && cell[k] < p.n_cells) ? 0u : kNoCellBit);
+                q.bev = cell[k];
+                q.pad = 0;
+                sm.rec[i] = q;
+                skip_any |= !ok;
             }
+        }
+        f0 = __reduce_min_sync(0xffffffffu, f0);
+        f1 = __reduce_min_sync(0xffffffffu, f1);
+        if (lane == 0) {
+            s_min[0][warp] = f0;
+            s_min[1][warp] = f1;
+        }
+        const bool checked = __syncthreads_or(skip_any);   // some point of the round is skipped
+        int m0 = INT_MAX, m1 = INT_MAX;
 #pragma unroll
-            for (int kk = 0; kk < S::BATCH; ++kk) {
-                fma_vec<DT, S::VB>(acc, d[kk], f[kk]);
-                if ((ends >> kk) & 1u) {                     // an interval ends with this point
-                    const int bev = __shfl_sync(gmask, rc, lane0 + kk);
-                    if (to_slot) {
-                        float *dst = &sm.slot[0][o][ol * S::EPL];
+        for (int w = 0; w < kWarps; ++w) {
+            m0 = min(m0, s_min[0][w]);
+            m1 = min(m1, s_min[1][w]);
+        }
+        if (T0 < 0) {
+            if (m0 == INT_MAX) {                   // the window lies inside one interval
+                cta_next_starts(p, n_pts, n_int, x0, x1, &T0, &T1, s_bounds);   // contains barriers
+                if (T1 <= T0) return;              // uniform: the CTA before owns these points
+                w0 = T0;                           // stage again from the chunk's first point
+                rnd = -1;
+                continue;
+            }
+            T0 = m0;
+        }
+        if (T1 < 0) {
+            if (m1 != INT_MAX) T1 = m1;
+            else if (w0 + W >= n_pts) T1 = n_pts;
+        }
+        if (T1 >= 0 && T1 <= T0) return;           // no interval starts in [x0, x1): the CTA before owns them
+        // the chunk's points in this window: records [lo, hi)
+        const int lo = max(T0, w0) - w0;
+        const int hi = (T1 >= 0 ? min(T1, w0 + W) : w0 + W) - w0;
+        const int R = hi - lo;
+        const bool first_head = T0 >= w0 ? true : round_head;
+
+        // 3. owners take equal shares of the round and walk them, U points
+        //    at a time.  A share that starts inside an interval leaves its
+        //    first partial row in its slot; a share that ends inside an
+        //    interval it started keeps that partial in registers and adds the
+        //    later owners' slots after the barrier.
+        const int share = (R + S::OWNERS * U - 1) / (S::OWNERS * U) * U;   // whole groups where possible
+        const int beg = lo + min(R, o * share);
+        const int end = lo + min(R, o * share + share);
+        const bool next_head = (sm.rec[W - 1].dflags & kEndBit) != 0u;
+        bool head_cut = false;                     // this owner finishes an interval cut by its share end
+        int head_bev = -1;
+        float acc[S::EPL];                         // after the walk: the partial row of that interval
+        if (active) {
+            int st = kEmpty;
+            if (beg < end) {
+                const bool head = beg == lo ? first_head : (sm.rec[beg - 1].dflags & kEndBit) != 0u;
+                bool to_slot = !head;              // the next finished segment continues a previous share
+#pragma unroll
+                for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
+                // n < U (a share's tail) or a round with skipped points: checked walk
+                auto walk = [&](int v, int n, auto full_tag) {
+                    constexpr bool FULL = decltype(full_tag)::value;
+                    int rows[U];
+                    uint32_t df[U];
+#pragma unroll
+                    for (int kk = 0; kk < U; ++kk) {
+                        if (FULL || kk < n) {
+                            const int4 q = *reinterpret_cast<const int4 *>(&sm.rec[v + kk]);
+                            rows[kk] = q.x;
+                            df[kk] = static_cast<uint32_t>(q.y);
+                        } else {
+                            rows[kk] = 0;
+                            df[kk] = kSkipBit;
+                        }
+                    }
+                    RawVec<S::VB> f[U];
+                    [[maybe_unused]] unsigned short sh[U];
+#pragma unroll
+                    for (int kk = 0; kk < U; ++kk) {
+                        if (FULL || kk < n) {              // skipped points load row 0 and add nothing
+                            f[kk] = load_vec<S::VB>(featp + static_cast<int64_t>(rows[kk]) * S::ROWB);
+                            if constexpr (S::NV) {
+                                const unsigned char sc = __ldg(blockp + static_cast<int64_t>(rows[kk]) * (C / 16));
+                                sh[kk] = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sc), __NV_E4M3).x;
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < RawVec<S::VB>::NW; ++i) f[kk].w[i] = 0u;
+                            if constexpr (S::NV) sh[kk] = 0;
+                        }
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < U; ++kk) {
+                        unsigned short d = static_cast<unsigned short>(df[kk] & 0xffffu);
+                        if constexpr (S::NV) d = mul_f16_bits(d, sh[kk]);   // depth x block scale (exact in fp16)
+                        if (FULL || !(df[kk] & kSkipBit)) fma_vec<DT, S::VB>(acc, d, f[kk]);
+                        if (df[kk] & kEndBit) {                // an interval ends with this point
+                            if (to_slot) {
+                                float *dst = &sm.slot[o][ol * S::EPL];
+#pragma unroll
+                                for (int e = 0; e < S::EPL; ++e) dst[e] = acc[e];
+                                to_slot = false;
+                            } else if (!(df[kk] & kNoCellBit)) {
+                                store_interval<OT, C, S::EPL>(p, sm.rec[v + kk].bev, ol, acc);
+                            }
+#pragma unroll
+                            for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
+                        }
+                    }
+                };
+                // software pipeline (not in the 64-register lean variant): the
+                // next group's rows are in flight while this group's FMAs run
+                // (two register buffers of PU points)
+                constexpr int PU = LEAN                   ? 0
+                                   : DT == kDtypeE4M3     ? BEVPOOL_FWD_PIPELINE_FP8
+                                   : DT == kDtypeNVFP4    ? BEVPOOL_FWD_PIPELINE_NVFP4
+                                                          : BEVPOOL_FWD_PIPELINE;
+                if constexpr (PU > 0) {
+                struct Grp {
+                    uint32_t df[PU];
+                    RawVec<S::VB> f[PU];
+                    [[maybe_unused]] unsigned short sh[PU];
+                };
+                auto fetch = [&](Grp &g, int v) {
+                    int rows[PU];
+#pragma unroll
+                    for (int kk = 0; kk < PU; ++kk) {
+                        if (v + kk < end) {
+                            const int2 q = *reinterpret_cast<const int2 *>(&sm.rec[v + kk]);
+                            rows[kk] = q.x;
+                            g.df[kk] = static_cast<uint32_t>(q.y);
+                        } else {
+                            rows[kk] = 0;
+                            g.df[kk] = kSkipBit;
+                        }
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < PU; ++kk) {
+                        if (v + kk < end) {
+                            g.f[kk] = load_vec<S::VB>(featp + static_cast<int64_t>(rows[kk]) * S::ROWB);
+                            if constexpr (S::NV) {
+                                const unsigned char sc = __ldg(blockp + static_cast<int64_t>(rows[kk]) * (C / 16));
+                                g.sh[kk] = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sc), __NV_E4M3).x;
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < RawVec<S::VB>::NW; ++i) g.f[kk].w[i] = 0u;
+                            if constexpr (S::NV) g.sh[kk] = 0;
+                        }
+                    }
+                };
+                auto consume = [&](const Grp &g, int v) {
+#pragma unroll
+                    for (int kk = 0; kk < PU; ++kk) {
+                        unsigned short d = static_cast<unsigned short>(g.df[kk] & 0xffffu);
+                        if constexpr (S::NV) d = mul_f16_bits(d, g.sh[kk]);
+                        if (!(g.df[kk] & kSkipBit)) fma_vec<DT, S::VB>(acc, d, g.f[kk]);
+                        if (g.df[kk] & kEndBit) {
+                            if (to_slot) {
+                                float *dst = &sm.slot[o][ol * S::EPL];
+#pragma unroll
+                                for (int e = 0; e < S::EPL; ++e) dst[e] = acc[e];
+                                to_slot = false;
+                            } else if (!(g.df[kk] & kNoCellBit)) {
+                                store_interval<OT, C, S::EPL>(p, sm.rec[v + kk].bev, ol, acc);
+                            }
+#pragma unroll
+                            for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
+                        }
+                    }
+                };
+                Grp ga, gb;
+                fetch(ga, beg);
+                for (int v = beg;;) {
+                    if (v + PU < end) fetch(gb, v + PU);
+                    consume(ga, v);
+                    v += PU;
+                    if (v >= end) break;
+                    if (v + PU < end) fetch(ga, v + PU);
+                    consume(gb, v);
+                    v += PU;
+                    if (v >= end) break;
+                }
+                } else {
+                    int v = beg;
+                    if (!checked) {
+                        for (; v + U <= end; v += U) walk(v, U, std::true_type{});
+                    }
+                    for (; v < end; v += U) walk(v, min(U, end - v), std::false_type{});
+                }
+                const bool cut = (sm.rec[end - 1].dflags & kEndBit) == 0u;   // the share ends inside an interval
+                st = head ? kHead : (to_slot && cut ? kPass : kCont);
+                if (cut) {
+                    if (to_slot) {                 // the whole share continues an earlier interval
+                        float *dst = &sm.slot[o][ol * S::EPL];
 #pragma unroll
                         for (int e = 0; e < S::EPL; ++e) dst[e] = acc[e];
-                        to_slot = false;
-                    } else if (bev >= 0 && bev < p.n_cells) {
-                        store_row_part<OT, S::EPL>(p.out + (static_cast<int64_t>(bev) * C + ol * S::EPL) * OB, acc,
-                                                   p.scale, p.streaming);
+                    } else {                       // acc keeps the interval's first part
+                        head_cut = true;
+                        head_bev = sm.rec[end - 1].bev;
                     }
-#pragma unroll
-                    for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
                 }
             }
-            rd = rd_next;
-            rf = rf_next;
-            rc = rc_next;
+            if (ol == 0) sm.state[o] = st;
         }
-        bool cut = false;                                    // the share ends inside an interval
-        if (beg < end && end < P) {
-            head_bev = __ldg(p.ranks_bev + T0 + end - 1);
-            cut = __ldg(p.ranks_bev + T0 + end) == head_bev;
-        }
-        int st = kHead;
-        if (!head) st = to_slot && cut ? kPass : kCont;
-        if (cut) {
-            float *dst = &sm.slot[to_slot ? 0 : 1][o][ol * S::EPL];
-#pragma unroll
-            for (int e = 0; e < S::EPL; ++e) dst[e] = acc[e];
-            head_cut = !to_slot;
-        }
-        if (ol == 0) sm.state[o] = st;
-    }
 
-    // 3. combine cut intervals in owner order (fixed order: deterministic)
-    __syncthreads();
-    if (head_cut) {
-        float acc[S::EPL];
-        const float *src = &sm.slot[1][o][ol * S::EPL];
+        // 4. combine cut intervals in owner order (fixed order: deterministic).
+        //    An interval still open at the round's end goes to the carry; the
+        //    first owner's lanes take the carry of the previous round.
+        __syncthreads();
+        // adds the slots of owners o2, o2 + 1, ... to a until one of them ends
+        // the interval (then stores it) or the round ends (then carries it)
+        auto finish = [&](float *a, int o2, int bev) {
+            for (; o2 < S::OWNERS; ++o2) {
+                const int st2 = sm.state[o2];
+                if (st2 == kHead || st2 == kEmpty) break;
+                const float *q = &sm.slot[o2][ol * S::EPL];
 #pragma unroll
-        for (int e = 0; e < S::EPL; ++e) acc[e] = src[e];
-        for (int o2 = o + 1; o2 < S::OWNERS; ++o2) {
-            const int st = sm.state[o2];
-            if (st == kHead) break;
-            const float *q = &sm.slot[0][o2][ol * S::EPL];
+                for (int e = 0; e < S::EPL; ++e) a[e] += q[e];
+                if (st2 == kCont) {
+                    if (bev >= 0 && bev < p.n_cells) store_interval<OT, C, S::EPL>(p, bev, ol, a);
+                    return;
+                }
+            }
+            float *dst = &sm.carry[cb ^ 1][ol * S::EPL];
 #pragma unroll
-            for (int e = 0; e < S::EPL; ++e) acc[e] += q[e];
-            if (st == kCont) break;
+            for (int e = 0; e < S::EPL; ++e) dst[e] = a[e];
+            if (ol == 0) sm.carry_bev[cb ^ 1] = bev;
+        };
+        if (!first_head && active && o == 0) {
+            float ca[S::EPL];
+            const float *src = &sm.carry[cb][ol * S::EPL];
+#pragma unroll
+            for (int e = 0; e < S::EPL; ++e) ca[e] = src[e];
+            finish(ca, 0, sm.carry_bev[cb]);
         }
-        if (head_bev >= 0 && head_bev < p.n_cells)
-            store_row_part<OT, S::EPL>(p.out + (static_cast<int64_t>(head_bev) * C + ol * S::EPL) * OB, acc,
-                                       p.scale, p.streaming);
+        if (head_cut) finish(acc, o + 1, head_bev);
+        if (T1 >= 0 && T1 <= w0 + W) break;        // uniform: the chunk ends in this window
+        round_head = next_head;
+        w0 += W;
+        __syncthreads();                           // the next round overwrites records, states and slots
     }
 }
 
@@ -685,6 +859,13 @@ cudaError_t launch_forward_v(const ForwardArgs &a) {
                            : (a.streaming_stores ? BEVPOOL_FWD_CTAS_PER_SM_DRAM : BEVPOOL_FWD_CTAS_PER_SM_L2));
     int64_t n_compute = div_up(a.n_points, static_cast<int64_t>(S::OWNERS) * S::BATCH);
     if (n_compute > slots) n_compute = slots;
+#if BEVPOOL_FWD_MULTIWAVE
+    if (!a.loose_capacity) {
+        const int64_t per_cta = ComputeSmem<DT, C, LEAN>::ROUND - BEVPOOL_FWD_MULTIWAVE;   // one round each
+        const int64_t want = div_up(a.n_points, per_cta);
+        if (want > n_compute) n_compute = slots * div_up(want, slots);   // whole waves
+    }
+#endif
     if (n_compute < 1) n_compute = 1;
     p.n_compute = static_cast<int>(n_compute);
     p.n_compute_div = FastDiv(static_cast<uint32_t>(n_compute));
@@ -702,12 +883,21 @@ cudaError_t launch_forward_v(const ForwardArgs &a) {
     return e;
 }
 
-// fp16 rows whose output streams to DRAM take the lean variant (measured: DRAM
-// batch 122.9 -> 114.7 us; with the output in L2 it was not faster).
+// fp16 rows take the lean variant when the output streams to DRAM (measured:
+// DRAM batch 122.9 -> 114.7 us) and when there is much work per SM even with
+// the output in L2 (n_points * C >= 2^17 per SM; measured warm-L2: 572K points
+// at C = 80 24.2 -> 21.8 us, 1.28M points 42.8 -> 38.9, 209K points at C = 128
+// 16.5 -> 15.3; below it slower: 182K points at C = 64 10.4 -> 13.4 us).
+// With the counts on the device n_points is the caller's capacity, which
+// stands in for the count unless it is the whole frustum (then it says
+// nothing about the frame's points).
 template <int DT, int C, int OT>
 cudaError_t launch_forward_t(const ForwardArgs &a) {
     if constexpr (DT == kDtypeF16) {
-        if (a.streaming_stores) return launch_forward_v<DT, C, OT, true>(a);
+        const int64_t sms = a.sm_count > 0 ? a.sm_count : 148;
+        const bool much_work =
+            !a.loose_capacity && a.n_points * static_cast<int64_t>(C) >= BEVPOOL_FWD_LEAN_WORK_PER_SM * sms;
+        if (a.streaming_stores || much_work) return launch_forward_v<DT, C, OT, true>(a);
     }
     return launch_forward_v<DT, C, OT, false>(a);
 }

@@ -315,6 +315,32 @@ BEVPOOL_API bevpool_status bevpool_validate_map(const int32_t *ranks_depth, cons
                                     int32_t W, int32_t n_cells, int32_t *d_result,
                                     int32_t *h_result, void *stream);
 
+/*
+ * L2 streaming probe (a measurement helper, not part of the pooling path):
+ * the bandwidth at which the SMs read, write or copy a buffer resident in L2,
+ * the denominator of the forward's roofline when its working set fits in L2
+ * (the pages' large-L2 regime, section "Optimize for large L2 caches").
+ * buf: device, 16-byte aligned; bytes at most 2^32.  One launch on `stream`;
+ * time it with events around the call, after one call that brings the
+ * buffer into L2.
+ *
+ * mode = 0 (read): reads the `bytes` of buf (a multiple of 16) `passes` times
+ *   with 16-byte L2-only loads and adds the sum of its 32-bit words (mod 2^32,
+ *   once per pass) to *d_sink (device uint32 the caller zeroes first), so
+ *   every byte is known to have been read.
+ * mode = 1 (write): writes buf (a multiple of 16 bytes) `passes` times with
+ *   16-byte stores; afterwards 32-bit word k holds k ^ ((passes - 1) * 0x9E3779B9)
+ *   (mod 2^32).
+ * mode = 2 (copy): bytes a multiple of 32; each pass reads the first half and
+ *   writes the second half; afterwards word k of the second half holds word k
+ *   of the first half ^ ((passes - 1) * 0x9E3779B9).  A pass moves `bytes`
+ *   (half read, half written), the convention of a STREAM copy.
+ * d_sink may be NULL for modes 1 and 2.  Returns BEVPOOL_ERR_INVALID_ARG for
+ * a bad argument (nothing launched), BEVPOOL_ERR_CUDA if the launch fails.
+ */
+BEVPOOL_API bevpool_status bevpool_probe_l2(int32_t mode, void *buf, size_t bytes, int32_t passes,
+                                uint32_t *d_sink, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

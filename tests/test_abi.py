@@ -160,3 +160,18 @@ def test_forward_nvfp4_rejects_bad_arguments(bp):
     for change in [dict(feat_block=0), dict(feat=FAKE + 8), dict(out_dtype=bp.BEVPOOL_E4M3, out_scale=0.0),
                    dict(NC=0)]:
         assert bp.bevpool_forward_nvfp4(**{**args, **change}) == bp.BEVPOOL_ERR_INVALID_ARG, change
+
+
+def test_probe_l2_rejects_bad_arguments(bp):
+    """Argument checks come before any CUDA call."""
+    fake = 1 << 20   # never dereferenced: every call below fails its checks first
+    assert bp.bevpool_probe_l2(3, fake, 64, 1, fake, 0) == bp.BEVPOOL_ERR_INVALID_ARG     # no such mode
+    assert bp.bevpool_probe_l2(-1, fake, 64, 1, fake, 0) == bp.BEVPOOL_ERR_INVALID_ARG
+    assert bp.bevpool_probe_l2(2, fake, 48, 1, 0, 0) == bp.BEVPOOL_ERR_INVALID_ARG        # copy: halves of 16 B
+    assert bp.bevpool_probe_l2(0, 0, 64, 1, fake, 0) == bp.BEVPOOL_ERR_INVALID_ARG        # NULL buffer
+    assert bp.bevpool_probe_l2(0, fake, 0, 1, fake, 0) == bp.BEVPOOL_ERR_INVALID_ARG      # empty
+    assert bp.bevpool_probe_l2(0, fake, 40, 1, fake, 0) == bp.BEVPOOL_ERR_INVALID_ARG     # not 16-byte multiple
+    assert bp.bevpool_probe_l2(0, fake + 8, 64, 1, fake, 0) == bp.BEVPOOL_ERR_INVALID_ARG  # misaligned
+    assert bp.bevpool_probe_l2(0, fake, 64, 0, fake, 0) == bp.BEVPOOL_ERR_INVALID_ARG     # no pass
+    assert bp.bevpool_probe_l2(0, fake, 64, 1, 0, 0) == bp.BEVPOOL_ERR_INVALID_ARG        # read without sink
+    assert bp.bevpool_probe_l2(1, fake, (1 << 32) + 16, 1, 0, 0) == bp.BEVPOOL_ERR_INVALID_ARG   # too large
