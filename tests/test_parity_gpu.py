@@ -263,3 +263,47 @@ def test_streaming_regime_channel_counts(bp, C):
     gpu_forward(wl, m, depth, feat, out=out)
     torch.cuda.synchronize()
     assert_forward_close(wl, out, oracle_forward(wl))
+
+
+def test_forward_skips_out_of_range_entries(bp, wl_cache):
+    """A map with out-of-range entries, as the forward's contract states:
+    a point whose ranks_depth / ranks_feat is outside the tensors adds
+    nothing, an interval whose cell is outside [0, n_cells) is not written
+    (its old cell is then written as zeros).  The expected output is the
+    oracle's on the same frustum with those points dropped, which gives the
+    same rows.  Runs the checked walk (skipped points) and the no-cell path."""
+    import oracle
+
+    wl = wl_cache("canonical")
+    cells, depth, feat = upload(wl)
+    m = _gpu_map(bp, wl, cells)
+    h = m.host()
+    n = h["n_points"]
+    rng = np.random.default_rng(5)
+    rd0 = h["ranks_depth"]
+    rd, rf, rb = rd0.copy(), h["ranks_feat"].copy(), h["ranks_bev"].copy()
+    bad_d = rng.choice(n, 300, replace=False)
+    bad_f = rng.choice(n, 300, replace=False)
+    rd[bad_d[:150]] = -3
+    rd[bad_d[150:]] = wl.n_frustum + 11
+    rf[bad_f[:150]] = -1
+    rf[bad_f[150:]] = wl.n_feat_rows
+    s, ln = h["interval_starts"], h["interval_lengths"]
+    first = np.arange(s[0], s[0] + ln[0])
+    last = np.arange(s[-1], s[-1] + ln[-1])
+    rb[first] = -7                                   # still ascending
+    rb[last] = wl.n_cells + 5
+    dropped = np.unique(np.concatenate([rd0[bad_d], rd0[bad_f], rd0[first], rd0[last]]))
+    m.ranks_depth[:n].copy_(torch.from_numpy(rd))
+    m.ranks_feat[:n].copy_(torch.from_numpy(rf))
+    m.ranks_bev[:n].copy_(torch.from_numpy(rb))
+    out = torch.full((wl.n_cells, wl.C), float("nan"), dtype=torch.float16, device="cuda")
+    gpu_forward(wl, m, depth, feat, out=out)
+    torch.cuda.synchronize()
+    cid = wl.cell_ids.copy()
+    cid[dropped] = -1
+    ref = oracle.forward(wl.dtype, cid, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat, wl.depth_scale,
+                         wl.feat_scale)
+    assert_forward_close(wl, out, ref)
+    g = out.float().cpu().numpy()
+    assert np.all(g[int(h["ranks_bev"][s[0]])] == 0) and np.all(g[int(h["ranks_bev"][s[-1]])] == 0)
