@@ -87,6 +87,9 @@
 #ifndef BEVPOOL_FWD_MULTIWAVE
 #define BEVPOOL_FWD_MULTIWAVE 64          // > 0: compute CTAs of at most a round less this many points each
 #endif
+#ifndef BEVPOOL_FWD_STORE_HINT
+#define BEVPOOL_FWD_STORE_HINT 1          // 1: output stores take an L2 cache policy instead of a branch
+#endif
 #ifndef BEVPOOL_FWD_LEAN_WORK_PER_SM
 #define BEVPOOL_FWD_LEAN_WORK_PER_SM 131072   // fp16 rows with at least this many point-channels per SM run lean
 #endif
@@ -287,15 +290,44 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+#if BEVPOOL_FWD_STORE_HINT
+// Output stores carry an L2 cache policy chosen once per thread (evict-first
+// when the output streams to DRAM, normal otherwise): one store instruction
+// either way, no branch at every interval end.
+using StoreMode = uint64_t;
+__device__ __forceinline__ StoreMode store_mode(bool streaming) {
+    uint64_t pol;
+    if (streaming)
+        asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    else
+        asm("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void store_vec(uint4 *p, const uint4 &v, StoreMode m) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w), "l"(m)
+                 : "memory");
+}
+__device__ __forceinline__ void store_vec(uint2 *p, const uint2 &v, StoreMode m) {
+    asm volatile("st.global.L2::cache_hint.v2.b32 [%0], {%1, %2}, %3;" ::"l"(p), "r"(v.x), "r"(v.y), "l"(m)
+                 : "memory");
+}
+__device__ __forceinline__ void store_vec(unsigned int *p, const unsigned int &v, StoreMode m) {
+    asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(m) : "memory");
+}
+#else
+using StoreMode = bool;                            // true: evict-first (streaming) stores
+__device__ __forceinline__ StoreMode store_mode(bool streaming) { return streaming; }
 template <typename V>
-__device__ __forceinline__ void store_vec(V *p, const V &v, bool streaming) {
+__device__ __forceinline__ void store_vec(V *p, const V &v, StoreMode streaming) {
     if (streaming) __stcs(p, v); else *p = v;
 }
+#endif
 
 // Store EPL channels, scaled and rounded to the output type, at dst
 // (EPL * element bytes, aligned to that size).
 template <int OT, int EPL>
-__device__ __forceinline__ void store_row_part(unsigned char *dst, const float *acc, float scale, bool streaming) {
+__device__ __forceinline__ void store_row_part(unsigned char *dst, const float *acc, float scale, StoreMode streaming) {
     if constexpr (OT == kOutF16) {
         constexpr int NW = EPL / 2;   // 32-bit words
         uint32_t w[NW];
@@ -453,9 +485,9 @@ __device__ __forceinline__ void cta_next_starts(const FwdParams &p, int n, int n
 // acc[0 .. EPL) of an interval: to the output row of cell bev (in range),
 // scaled and rounded.
 template <int OT, int C, int EPL>
-__device__ __forceinline__ void store_interval(const FwdParams &p, int bev, int ol, const float *acc) {
+__device__ __forceinline__ void store_interval(const FwdParams &p, int bev, int ol, const float *acc, StoreMode mode) {
     constexpr int OB = OT == kOutF16 ? 2 : 1;
-    store_row_part<OT, EPL>(p.out + (static_cast<int64_t>(bev) * C + ol * EPL) * OB, acc, p.scale, p.streaming);
+    store_row_part<OT, EPL>(p.out + (static_cast<int64_t>(bev) * C + ol * EPL) * OB, acc, p.scale, mode);
 }
 
 template <int DT, int C, int OT, bool LEAN>
@@ -491,6 +523,7 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
     const int o = active ? warp * S::OPW + og : 0;
     const unsigned char *featp = static_cast<const unsigned char *>(p.feat) + ol * S::VB;
     [[maybe_unused]] const unsigned char *blockp = p.feat_block + ol;   // NVFP4: the lane's block scale
+    const StoreMode mode = store_mode(p.streaming != 0);
 
     int T0 = -1, T1 = -1;                          // known once found (uniform over the CTA)
     int w0 = x0;                                   // first point of the staged window
@@ -639,7 +672,7 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
                                 for (int e = 0; e < S::EPL; ++e) dst[e] = acc[e];
                                 to_slot = false;
                             } else if (!(df[kk] & kNoCellBit)) {
-                                store_interval<OT, C, S::EPL>(p, sm.rec[v + kk].bev, ol, acc);
+                                store_interval<OT, C, S::EPL>(p, sm.rec[v + kk].bev, ol, acc, mode);
                             }
 #pragma unroll
                             for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
@@ -700,7 +733,7 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
                                 for (int e = 0; e < S::EPL; ++e) dst[e] = acc[e];
                                 to_slot = false;
                             } else if (!(g.df[kk] & kNoCellBit)) {
-                                store_interval<OT, C, S::EPL>(p, sm.rec[v + kk].bev, ol, acc);
+                                store_interval<OT, C, S::EPL>(p, sm.rec[v + kk].bev, ol, acc, mode);
                             }
 #pragma unroll
                             for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
@@ -756,7 +789,7 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
 #pragma unroll
                 for (int e = 0; e < S::EPL; ++e) a[e] += q[e];
                 if (st2 == kCont) {
-                    if (bev >= 0 && bev < p.n_cells) store_interval<OT, C, S::EPL>(p, bev, ol, a);
+                    if (bev >= 0 && bev < p.n_cells) store_interval<OT, C, S::EPL>(p, bev, ol, a, mode);
                     return;
                 }
             }
@@ -802,13 +835,11 @@ __device__ __forceinline__ void fill_cta(const FwdParams &p, int fidx, FillSmem 
     const int total = (c1 - c0) * OUT_VECS;
     uint4 *out = reinterpret_cast<uint4 *>(p.out + static_cast<int64_t>(c0) * OUT_VECS * 16);
     const uint4 z = make_uint4(0, 0, 0, 0);
+    const StoreMode mode = store_mode(p.streaming != 0);
     for (int v = threadIdx.x; v < total; v += kThreads) {
         const int cell = v / OUT_VECS;
         if (!((sm.mark[cell >> 5] >> (cell & 31)) & 1u)) {
-            if (p.streaming)
-                __stcs(out + v, z);
-            else
-                out[v] = z;
+            store_vec(out + v, z, mode);
         }
     }
 }
