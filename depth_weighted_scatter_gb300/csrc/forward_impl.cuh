@@ -292,8 +292,8 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
 
 #if BEVPOOL_FWD_STORE_HINT
 // Output stores carry an L2 cache policy chosen once per thread (evict-first
-// when the output streams to DRAM, normal otherwise): one store instruction
-// either way, no branch at every interval end.
+// when the output streams to DRAM, normal otherwise) and a predicate (whether
+// to store at all): one store instruction, no branch at every interval end.
 using StoreMode = uint64_t;
 __device__ __forceinline__ StoreMode store_mode(bool streaming) {
     uint64_t pol;
@@ -303,23 +303,30 @@ __device__ __forceinline__ StoreMode store_mode(bool streaming) {
         asm("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
-__device__ __forceinline__ void store_vec(uint4 *p, const uint4 &v, StoreMode m) {
-    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w), "l"(m)
+__device__ __forceinline__ void store_vec(uint4 *p, const uint4 &v, StoreMode m, bool on = true) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %6, 0;\n\t"
+                 "@q st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;\n\t}" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w), "l"(m), "r"(static_cast<unsigned>(on))
                  : "memory");
 }
-__device__ __forceinline__ void store_vec(uint2 *p, const uint2 &v, StoreMode m) {
-    asm volatile("st.global.L2::cache_hint.v2.b32 [%0], {%1, %2}, %3;" ::"l"(p), "r"(v.x), "r"(v.y), "l"(m)
+__device__ __forceinline__ void store_vec(uint2 *p, const uint2 &v, StoreMode m, bool on = true) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %4, 0;\n\t"
+                 "@q st.global.L2::cache_hint.v2.b32 [%0], {%1, %2}, %3;\n\t}" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "l"(m), "r"(static_cast<unsigned>(on))
                  : "memory");
 }
-__device__ __forceinline__ void store_vec(unsigned int *p, const unsigned int &v, StoreMode m) {
-    asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(m) : "memory");
+__device__ __forceinline__ void store_vec(unsigned int *p, const unsigned int &v, StoreMode m, bool on = true) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %3, 0;\n\t"
+                 "@q st.global.L2::cache_hint.b32 [%0], %1, %2;\n\t}" ::"l"(p), "r"(v), "l"(m),
+                 "r"(static_cast<unsigned>(on))
+                 : "memory");
 }
 #else
 using StoreMode = bool;                            // true: evict-first (streaming) stores
 __device__ __forceinline__ StoreMode store_mode(bool streaming) { return streaming; }
 template <typename V>
-__device__ __forceinline__ void store_vec(V *p, const V &v, StoreMode streaming) {
+__device__ __forceinline__ void store_vec(V *p, const V &v, StoreMode streaming, bool on = true) {
+    if (!on) return;
     if (streaming) __stcs(p, v); else *p = v;
 }
 #endif
@@ -327,26 +334,22 @@ __device__ __forceinline__ void store_vec(V *p, const V &v, StoreMode streaming)
 // Store EPL channels, scaled and rounded to the output type, at dst
 // (EPL * element bytes, aligned to that size).
 template <int OT, int EPL>
-__device__ __forceinline__ void store_row_part(unsigned char *dst, const float *acc, float scale, StoreMode streaming) {
+__device__ __forceinline__ void store_row_part(unsigned char *dst, const float *acc, float scale, StoreMode streaming,
+                                               bool on = true) {
     if constexpr (OT == kOutF16) {
         constexpr int NW = EPL / 2;   // 32-bit words
         uint32_t w[NW];
-        if (scale == 1.f) {                        // x * 1 == x: skip the multiplies (the usual fp16 case)
 #pragma unroll
-            for (int i = 0; i < NW; ++i) w[i] = pack_half2(acc[2 * i], acc[2 * i + 1]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < NW; ++i) w[i] = pack_half2(acc[2 * i] * scale, acc[2 * i + 1] * scale);
-        }
+        for (int i = 0; i < NW; ++i) w[i] = pack_half2(acc[2 * i] * scale, acc[2 * i + 1] * scale);
         if constexpr (NW % 4 == 0) {
 #pragma unroll
             for (int q = 0; q < NW / 4; ++q)
                 store_vec(reinterpret_cast<uint4 *>(dst) + q,
-                          make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]), streaming);
+                          make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]), streaming, on);
         } else if constexpr (NW == 2) {
-            store_vec(reinterpret_cast<uint2 *>(dst), make_uint2(w[0], w[1]), streaming);
+            store_vec(reinterpret_cast<uint2 *>(dst), make_uint2(w[0], w[1]), streaming, on);
         } else {
-            store_vec(reinterpret_cast<unsigned int *>(dst), w[0], streaming);
+            store_vec(reinterpret_cast<unsigned int *>(dst), w[0], streaming, on);
         }
     } else {
         static_assert(EPL % 4 == 0, "E4M3 rows are stored four codes at a time");
@@ -364,11 +367,11 @@ __device__ __forceinline__ void store_row_part(unsigned char *dst, const float *
 #pragma unroll
             for (int q = 0; q < NW / 4; ++q)
                 store_vec(reinterpret_cast<uint4 *>(dst) + q,
-                          make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]), streaming);
+                          make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]), streaming, on);
         } else if constexpr (NW == 2) {
-            store_vec(reinterpret_cast<uint2 *>(dst), make_uint2(w[0], w[1]), streaming);
+            store_vec(reinterpret_cast<uint2 *>(dst), make_uint2(w[0], w[1]), streaming, on);
         } else {
-            store_vec(reinterpret_cast<unsigned int *>(dst), w[0], streaming);
+            store_vec(reinterpret_cast<unsigned int *>(dst), w[0], streaming, on);
         }
     }
 }
@@ -482,12 +485,13 @@ __device__ __forceinline__ void cta_next_starts(const FwdParams &p, int n, int n
     *t1 = min(max(r1, *t0), n);
 }
 
-// acc[0 .. EPL) of an interval: to the output row of cell bev (in range),
-// scaled and rounded.
+// acc[0 .. EPL) of an interval: to the output row of cell bev, scaled and
+// rounded; nothing is stored unless `on` (the cell is in range).
 template <int OT, int C, int EPL>
-__device__ __forceinline__ void store_interval(const FwdParams &p, int bev, int ol, const float *acc, StoreMode mode) {
+__device__ __forceinline__ void store_interval(const FwdParams &p, int bev, int ol, const float *acc, StoreMode mode,
+                                               bool on) {
     constexpr int OB = OT == kOutF16 ? 2 : 1;
-    store_row_part<OT, EPL>(p.out + (static_cast<int64_t>(bev) * C + ol * EPL) * OB, acc, p.scale, mode);
+    store_row_part<OT, EPL>(p.out + (static_cast<int64_t>(bev) * C + ol * EPL) * OB, acc, p.scale, mode, on);
 }
 
 template <int DT, int C, int OT, bool LEAN>
@@ -671,8 +675,9 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
 #pragma unroll
                                 for (int e = 0; e < S::EPL; ++e) dst[e] = acc[e];
                                 to_slot = false;
-                            } else if (!(df[kk] & kNoCellBit)) {
-                                store_interval<OT, C, S::EPL>(p, sm.rec[v + kk].bev, ol, acc, mode);
+                            } else {
+                                store_interval<OT, C, S::EPL>(p, sm.rec[v + kk].bev, ol, acc, mode,
+                                                              !(df[kk] & kNoCellBit));
                             }
 #pragma unroll
                             for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
@@ -732,8 +737,9 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
 #pragma unroll
                                 for (int e = 0; e < S::EPL; ++e) dst[e] = acc[e];
                                 to_slot = false;
-                            } else if (!(g.df[kk] & kNoCellBit)) {
-                                store_interval<OT, C, S::EPL>(p, sm.rec[v + kk].bev, ol, acc, mode);
+                            } else {
+                                store_interval<OT, C, S::EPL>(p, sm.rec[v + kk].bev, ol, acc, mode,
+                                                              !(g.df[kk] & kNoCellBit));
                             }
 #pragma unroll
                             for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
@@ -789,7 +795,7 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
 #pragma unroll
                 for (int e = 0; e < S::EPL; ++e) a[e] += q[e];
                 if (st2 == kCont) {
-                    if (bev >= 0 && bev < p.n_cells) store_interval<OT, C, S::EPL>(p, bev, ol, a, mode);
+                    store_interval<OT, C, S::EPL>(p, bev, ol, a, mode, bev >= 0 && bev < p.n_cells);
                     return;
                 }
             }
