@@ -72,6 +72,9 @@
 #ifndef BEVPOOL_FWD_LEAN_BATCH
 #define BEVPOOL_FWD_LEAN_BATCH 6          // fp16 rows, output streaming to DRAM: points in flight per owner
 #endif
+#ifndef BEVPOOL_FWD_E4M3_LEAN_BATCH
+#define BEVPOOL_FWD_E4M3_LEAN_BATCH 4     // E4M3 rows in the lean variant (output streaming to DRAM)
+#endif
 #ifndef BEVPOOL_FWD_LEAN_MIN_CTAS
 #define BEVPOOL_FWD_LEAN_MIN_CTAS 4       // ... with four CTAs per SM (64 registers), all computing
 #endif
@@ -133,6 +136,7 @@ struct FwdShape {
     static constexpr int BATCH_CFG = NV                                  ? BEVPOOL_FWD_NVFP4_BATCH
                                      : VB >= 32                          ? BEVPOOL_FWD_BATCH32
                                      : (DT == kDtypeF16 && LEAN)         ? BEVPOOL_FWD_LEAN_BATCH
+                                     : (DT == kDtypeE4M3 && LEAN)        ? BEVPOOL_FWD_E4M3_LEAN_BATCH
                                      : (DT == kDtypeF16 || VB < 16)      ? BEVPOOL_FWD_BATCH
                                                                          : BEVPOOL_FWD_E4M3_BATCH16;
     static constexpr int BATCH = BATCH_CFG;                       // points in flight per owner
@@ -928,8 +932,14 @@ cudaError_t launch_forward_v(const ForwardArgs &a) {
 // With the counts on the device n_points is the caller's capacity, which
 // stands in for the count unless it is the whole frustum (then it says
 // nothing about the frame's points).
+// E4M3 rows take it when the output streams to DRAM (wide C = 256: 21.1 -> 20.1
+// us warm); with the output in L2 it was mixed (572K points 20.7 -> 18.7,
+// 1.28M points 39.4 -> 41.0, C = 128 13.7 -> 14.0).
 template <int DT, int C, int OT>
 cudaError_t launch_forward_t(const ForwardArgs &a) {
+    if constexpr (DT == kDtypeE4M3) {
+        if (a.streaming_stores) return launch_forward_v<DT, C, OT, true>(a);
+    }
     if constexpr (DT == kDtypeF16) {
         const int64_t sms = a.sm_count > 0 ? a.sm_count : 148;
         const bool much_work =

@@ -240,11 +240,12 @@ def test_forward_rejects_bad_arguments(bp, wl_cache):
     assert ei.value.status == bp.BEVPOOL_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("dtype", ["f16", "e4m3"])
 @pytest.mark.parametrize("C", [8, 80, 256])
-def test_streaming_regime_channel_counts(bp, C):
+def test_streaming_regime_channel_counts(bp, C, dtype):
     """A grid big enough that the output streams past L2 selects the kernels
-    for that regime (evict-first stores; for fp16 the variant with four CTAs
-    per SM): parity on every row, the few occupied ones and the many zeros."""
+    for that regime (evict-first stores; the variant with four CTAs per SM):
+    parity on every row, the few occupied ones and the many zeros."""
     from depth_weighted_scatter_gb300 import workloads
 
     cells = (72 << 20) // (2 * C) + 1                   # > 72 MiB of fp16 output
@@ -255,7 +256,7 @@ def test_streaming_regime_channel_counts(bp, C):
     hot = rng.random(nf) < 0.3
     cid[hot] = rng.integers(0, 50, int(hot.sum()))      # a dense corner with long intervals
     cid[rng.random(nf) < 0.2] = -1
-    wl = workloads.custom(NC, D, H, W, C, cells, cid, seed=C, name=f"stream_C{C}")
+    wl = workloads.custom(NC, D, H, W, C, cells, cid, seed=C, dtype=dtype, name=f"stream_C{C}_{dtype}")
     c_d, depth, feat = upload(wl)
     m = _gpu_map(bp, wl, c_d)
     _check_map(bp, wl, m)
