@@ -31,3 +31,47 @@ def test_reference_arm_e4m3_output_and_nvfp4():
     d = _run("--impl", "reference", "--config", "table1_small_nvfp4", "--steps", "1", "--warmup", "0",
              "--out-dtype", "e4m3")
     assert d["value"] > 0 and "output" in d["config"]
+
+
+def test_forward_source_hash_ignores_comments_only(tmp_path, monkeypatch):
+    """The ncu traffic records stay valid across comment edits of the forward
+    sources and lapse on any code change."""
+    import shutil
+    import importlib.util
+
+    csrc = os.path.join(ROOT, "depth_weighted_scatter_gb300", "csrc")
+    fake_root = tmp_path
+    dst = fake_root / "depth_weighted_scatter_gb300" / "csrc"
+    dst.mkdir(parents=True)
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    for f in bench.FORWARD_SOURCES:
+        shutil.copy(os.path.join(csrc, f), dst / f)
+    monkeypatch.setattr(bench, "ROOT", str(fake_root))
+    h0 = bench.forward_source_hash()
+    impl = dst / "forward_impl.cuh"
+    text = impl.read_text()
+    impl.write_text(text.replace("// forward_impl.cuh --", "// forward_impl.cuh (edited comment) --", 1)
+                    + "\n/* a block comment */\n")
+    assert bench.forward_source_hash() == h0
+    impl.write_text(text.replace("constexpr int kFillCellsMin = 256;", "constexpr int kFillCellsMin = 512;", 1))
+    assert bench.forward_source_hash() != h0
+
+
+def test_bytes_model_matches_the_stated_formula():
+    """Footprint and gather bytes of the canonical workload as the design notes state them."""
+    import importlib.util
+
+    spec = importlib.util.spec_from_file_location("bench_under_test2", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    from depth_weighted_scatter_gb300 import workloads
+
+    wl = workloads.make("canonical")
+    import oracle
+
+    m = oracle.build_map(wl.cell_ids, *wl.dims(), wl.n_cells)
+    bm = bench.bytes_model(wl, m["n_points"], m["n_intervals"])
+    assert bm["footprint"] == 30_394_964
+    assert bm["gather"] == 57_574_622
