@@ -78,6 +78,9 @@
 #ifndef BEVPOOL_FWD_SHORT_BATCH
 #define BEVPOOL_FWD_SHORT_BATCH 6         // fp16 rows, short intervals: points in flight per owner (80 registers)
 #endif
+#ifndef BEVPOOL_FWD_LEAN_SHORT_BATCH
+#define BEVPOOL_FWD_LEAN_SHORT_BATCH 4    // fp16 rows, lean variant with short intervals
+#endif
 #ifndef BEVPOOL_FWD_LEAN_MIN_CTAS
 #define BEVPOOL_FWD_LEAN_MIN_CTAS 4       // ... with four CTAs per SM (64 registers), all computing
 #endif
@@ -121,14 +124,16 @@ constexpr int kFillCellsMax = 1024;
 
 // Kernel variants (a template parameter): the default; lean (fewer points in
 // flight, 64 registers, four compute CTAs per SM); short (fp16 rows whose
-// intervals are short on average: fewer points in flight at 80 registers).
+// intervals are short on average: fewer points in flight at 80 registers);
+// lean-short (the lean variant for fp16 rows with short intervals).
 constexpr int kVarDefault = 0;
 constexpr int kVarLean = 1;
 constexpr int kVarShort = 2;
+constexpr int kVarLeanShort = 3;
 
 template <int DT, int C, int VAR = 0>
 struct FwdShape {
-    static constexpr bool LEAN = VAR == kVarLean;
+    static constexpr bool LEAN = VAR == kVarLean || VAR == kVarLeanShort;
     static constexpr bool SHORT = VAR == kVarShort;
     static constexpr bool NV = DT == kDtypeNVFP4;
     static constexpr int EB = DT == kDtypeF16 ? 2 : 1;          // input bytes per element (E4M3)
@@ -144,6 +149,7 @@ struct FwdShape {
     static constexpr int OWNERS = kWarps * OPW;                 // owners per CTA
     static constexpr int BATCH_CFG = NV                                  ? BEVPOOL_FWD_NVFP4_BATCH
                                      : VB >= 32                          ? BEVPOOL_FWD_BATCH32
+                                     : (DT == kDtypeF16 && VAR == kVarLeanShort) ? BEVPOOL_FWD_LEAN_SHORT_BATCH
                                      : (DT == kDtypeF16 && LEAN)         ? BEVPOOL_FWD_LEAN_BATCH
                                      : (DT == kDtypeF16 && SHORT)        ? BEVPOOL_FWD_SHORT_BATCH
                                      : (DT == kDtypeE4M3 && LEAN)        ? BEVPOOL_FWD_E4M3_LEAN_BATCH
@@ -868,7 +874,7 @@ __device__ __forceinline__ void fill_cta(const FwdParams &p, int fidx, FillSmem 
 // ---------------------------------------------------------------- kernel
 
 template <int DT, int C, int OT, int VAR>
-__global__ void __launch_bounds__(kThreads, VAR == kVarLean ? BEVPOOL_FWD_LEAN_MIN_CTAS : BEVPOOL_FWD_MIN_CTAS)
+__global__ void __launch_bounds__(kThreads, FwdShape<DT, C, VAR>::LEAN ? BEVPOOL_FWD_LEAN_MIN_CTAS : BEVPOOL_FWD_MIN_CTAS)
     k_forward(const FwdParams p) {
     grid_dep_wait();                               // the map build may still be draining (dependent launch)
     grid_dep_allow();
@@ -956,12 +962,19 @@ cudaError_t launch_forward_t(const ForwardArgs &a) {
         const int64_t sms = a.sm_count > 0 ? a.sm_count : 148;
         const bool much_work =
             !a.loose_capacity && a.n_points * static_cast<int64_t>(C) >= BEVPOOL_FWD_LEAN_WORK_PER_SM * sms;
-        if (a.streaming_stores || much_work) return launch_forward_v<DT, C, OT, kVarLean>(a);
         // short intervals (fewer than 8 points on average, host counts or a
-        // capacity close to them): 6 points in flight per owner measured faster
-        // (canonical 11.0 -> 10.4 us warm; 19-point intervals 10.0 -> 10.4 us)
-        if (!a.loose_capacity && a.n_intervals > 0 && a.n_points < 8 * static_cast<int64_t>(a.n_intervals))
-            return launch_forward_v<DT, C, OT, kVarShort>(a);
+        // capacity close to them) take fewer points in flight per owner
+        const bool short_intervals =
+            !a.loose_capacity && a.n_intervals > 0 && a.n_points < 8 * static_cast<int64_t>(a.n_intervals);
+        // lean: 4 points in flight with short intervals (DRAM batch, 3.0 points
+        // per interval, 94.2 -> 92.5 us; C = 128 at 3.6 points 20.7 -> 20.5 us),
+        // else 6 (8.7-point intervals 25.3 -> 26.6 us at 4)
+        if (a.streaming_stores || much_work)
+            return short_intervals ? launch_forward_v<DT, C, OT, kVarLeanShort>(a)
+                                   : launch_forward_v<DT, C, OT, kVarLean>(a);
+        // 6 points in flight at 80 registers (canonical 11.0 -> 10.4 us warm;
+        // 19-point intervals 10.0 -> 10.4 us)
+        if (short_intervals) return launch_forward_v<DT, C, OT, kVarShort>(a);
     }
     return launch_forward_v<DT, C, OT, kVarDefault>(a);
 }

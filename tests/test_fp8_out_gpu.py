@@ -63,20 +63,48 @@ def test_dram_batch_e4m3_out_sampled(bp, wl_cache):
     assert np.all(np.abs(gv - v) <= np.maximum(np.abs(v) * 2.0 ** -3, 2.0 ** -9))
 
 
+@pytest.mark.parametrize("intervals", ["short", "long"])
 @pytest.mark.parametrize("dtype", ["f16", "e4m3"])
 @pytest.mark.parametrize("C", [16, 32, 64, 80, 96, 128, 160, 192, 256])
-def test_every_channel_count_e4m3_out(bp, C, dtype):
+def test_every_channel_count_e4m3_out(bp, C, dtype, intervals):
+    """Intervals of about 3 points (short) and of about 60 (long) select
+    different fp16 kernel variants."""
     from depth_weighted_scatter_gb300 import workloads
 
     NC, D, H, W, cells = 3, 17, 6, 11, 700
-    rng = np.random.default_rng(C * 11 + (dtype == "e4m3"))
+    rng = np.random.default_rng(C * 11 + (dtype == "e4m3") + 1000 * (intervals == "long"))
     nf = NC * D * H * W
-    cid = rng.integers(0, cells, nf).astype(np.int32)
+    cid = rng.integers(0, cells if intervals == "short" else 40, nf).astype(np.int32)
     cid[rng.random(nf) < 0.3] = -1
     cid[rng.random(nf) < 0.08] = 123
-    wl = workloads.custom(NC, D, H, W, C, cells, cid, seed=C + 1, dtype=dtype, name=f"C{C}_{dtype}_q")
+    wl = workloads.custom(NC, D, H, W, C, cells, cid, seed=C + 1, dtype=dtype, name=f"C{C}_{dtype}_{intervals}_q")
     s = _calibrated_scale(wl)
-    out, _ = _run(bp, wl, s)
+    out, m = _run(bp, wl, s)
+    assert (m.n_points < 8 * m.n_intervals) == (intervals == "short"), (m.n_points, m.n_intervals)
+    assert_e4m3_out_matches(wl, out, s)
+
+
+@pytest.mark.parametrize("intervals", ["short", "long"])
+@pytest.mark.parametrize("dtype", ["f16", "e4m3"])
+def test_streaming_regime_e4m3_out(bp, dtype, intervals):
+    """An E4M3 output larger than half of L2 takes the streaming kernels (four
+    CTAs per SM; for fp16 rows one variant for short intervals and one for
+    long): every row checked, the few occupied ones and the many zeros."""
+    from depth_weighted_scatter_gb300 import workloads
+
+    C = 128
+    cells = (72 << 20) // C + 1                          # > 72 MiB of E4M3 output
+    NC, D, H, W = 2, 11, 9, 13
+    rng = np.random.default_rng(91 + (dtype == "e4m3") + 1000 * (intervals == "long"))
+    nf = NC * D * H * W
+    cid = rng.integers(0, cells, nf).astype(np.int32)
+    hot = rng.random(nf) < (0.3 if intervals == "short" else 0.97)
+    cid[hot] = rng.integers(0, 50, int(hot.sum()))
+    cid[rng.random(nf) < 0.2] = -1
+    wl = workloads.custom(NC, D, H, W, C, cells, cid, seed=5, dtype=dtype, name=f"stream_q_{dtype}_{intervals}")
+    s = _calibrated_scale(wl)
+    out, m = _run(bp, wl, s)
+    assert (m.n_points < 8 * m.n_intervals) == (intervals == "short"), (m.n_points, m.n_intervals)
     assert_e4m3_out_matches(wl, out, s)
 
 

@@ -104,20 +104,31 @@ def test_forward_on_oracle_map(bp, wl_cache):
 SUPPORTED_C = [8, 16, 32, 64, 80, 96, 128, 160, 192, 256]
 
 
+def _check_interval_mix(m, intervals):
+    """The kernel variant depends on the mean interval length (fewer than 8
+    points per interval counts as short): check the case is on the intended side."""
+    n_pts, n_int = m.n_points, m.n_intervals
+    assert (n_pts < 8 * n_int) == (intervals == "short"), (n_pts, n_int)
+
+
+@pytest.mark.parametrize("intervals", ["short", "long"])
 @pytest.mark.parametrize("dtype", ["f16", "e4m3"])
 @pytest.mark.parametrize("C", SUPPORTED_C)
-def test_every_channel_count(bp, C, dtype):
+def test_every_channel_count(bp, C, dtype, intervals):
+    """Every channel count, with intervals of about 3 points (short) and of
+    about 60 (long): the two select different fp16 kernel variants."""
     from depth_weighted_scatter_gb300 import workloads
 
     NC, D, H, W, cells = 3, 17, 6, 11, 700
-    rng = np.random.default_rng(C * 7 + (dtype == "e4m3"))
+    rng = np.random.default_rng(C * 7 + (dtype == "e4m3") + 1000 * (intervals == "long"))
     nf = NC * D * H * W
-    cid = rng.integers(0, cells, nf).astype(np.int32)
+    cid = rng.integers(0, cells if intervals == "short" else 40, nf).astype(np.int32)
     cid[rng.random(nf) < 0.3] = -1
     cid[rng.random(nf) < 0.08] = 123                 # one long interval (several owners share it)
-    wl = workloads.custom(NC, D, H, W, C, cells, cid, seed=C, dtype=dtype, name=f"C{C}_{dtype}")
+    wl = workloads.custom(NC, D, H, W, C, cells, cid, seed=C, dtype=dtype, name=f"C{C}_{dtype}_{intervals}")
     c_d, depth, feat = upload(wl)
     m = _gpu_map(bp, wl, c_d)
+    _check_interval_mix(m, intervals)
     _check_map(bp, wl, m)
     out = torch.full((cells, C), float("nan"), dtype=torch.float16, device="cuda")
     gpu_forward(wl, m, depth, feat, out=out)
@@ -240,25 +251,29 @@ def test_forward_rejects_bad_arguments(bp, wl_cache):
     assert ei.value.status == bp.BEVPOOL_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("intervals", ["short", "long"])
 @pytest.mark.parametrize("dtype", ["f16", "e4m3"])
 @pytest.mark.parametrize("C", [8, 80, 256])
-def test_streaming_regime_channel_counts(bp, C, dtype):
+def test_streaming_regime_channel_counts(bp, C, dtype, intervals):
     """A grid big enough that the output streams past L2 selects the kernels
-    for that regime (evict-first stores; the variant with four CTAs per SM):
-    parity on every row, the few occupied ones and the many zeros."""
+    for that regime (evict-first stores; the variants with four CTAs per SM,
+    one for short intervals and one for long): parity on every row, the few
+    occupied ones and the many zeros."""
     from depth_weighted_scatter_gb300 import workloads
 
     cells = (72 << 20) // (2 * C) + 1                   # > 72 MiB of fp16 output
     NC, D, H, W = 2, 11, 9, 13
-    rng = np.random.default_rng(C + 77)
+    rng = np.random.default_rng(C + 77 + 1000 * (intervals == "long"))
     nf = NC * D * H * W
     cid = rng.integers(0, cells, nf).astype(np.int32)
-    hot = rng.random(nf) < 0.3
+    hot = rng.random(nf) < (0.3 if intervals == "short" else 0.97)
     cid[hot] = rng.integers(0, 50, int(hot.sum()))      # a dense corner with long intervals
     cid[rng.random(nf) < 0.2] = -1
-    wl = workloads.custom(NC, D, H, W, C, cells, cid, seed=C, dtype=dtype, name=f"stream_C{C}_{dtype}")
+    wl = workloads.custom(NC, D, H, W, C, cells, cid, seed=C, dtype=dtype,
+                          name=f"stream_C{C}_{dtype}_{intervals}")
     c_d, depth, feat = upload(wl)
     m = _gpu_map(bp, wl, c_d)
+    _check_interval_mix(m, intervals)
     _check_map(bp, wl, m)
     out = torch.full((cells, C), float("nan"), dtype=torch.float16, device="cuda")
     gpu_forward(wl, m, depth, feat, out=out)
