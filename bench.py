@@ -30,6 +30,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -241,6 +242,25 @@ def oracle_call(wl, out_scale=None):
                                            wl.depth_scale, wl.feat_scale, out_scale)
 
 
+def host_cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine() or "unknown"
+
+
 def cpu_oracle_time(wl, budget_s: float = 10.0, max_reps: int = 50, out_scale=None) -> dict:
     """Times the oracle's forward on the full workload, single-threaded."""
     import oracle
@@ -255,6 +275,7 @@ def cpu_oracle_time(wl, budget_s: float = 10.0, max_reps: int = 50, out_scale=No
         call()
         times.append(time.perf_counter() - t0)
     return {"value": statistics.mean(times) * 1e6, "unit": "us/call", "cores": 1, "kind": "oracle",
+            "median": statistics.median(times) * 1e6, "cpu_model": host_cpu_model(),
             "sample": f"full {wl.name} workload ({wl.n_kept} points, C={wl.C}), {len(times)} calls of the "
                       f"single-threaded FP64 C oracle forward; host has {os.cpu_count()} cores"}
 
@@ -287,7 +308,9 @@ def run_reference(args) -> None:
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_dict(wl, m["n_points"], m["n_intervals"], world, args.out_dtype),
             "cpu_baseline": {"value": v, "unit": "us/call", "cores": 1, "kind": "oracle",
-                             "sample": f"each step one full {wl.name} forward of the single-threaded FP64 C oracle"},
+                             "median": statistics.median(times) * 1e6, "cpu_model": host_cpu_model(),
+                             "sample": f"each step one full {wl.name} forward of the single-threaded FP64 C oracle; "
+                                       f"host has {os.cpu_count()} cores"},
             "e2e": {"value": v, "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

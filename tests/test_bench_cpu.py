@@ -24,6 +24,7 @@ def test_reference_arm_json_line():
         assert k in d, k
     assert d["impl"] == "reference" and d["higher_is_better"] is False and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["cpu_baseline"]["cpu_model"] and d["cpu_baseline"]["median"] > 0
     assert "workload" in d["config"]
 
 
