@@ -1,11 +1,13 @@
 // forward_impl.cuh -- the BEV-pooling forward kernel (sm_103a), templated on
-// input dtype and channel count.  Included by forward_f16.cu / forward_e4m3.cu.
+// input dtype, channel count, output type and kernel variant.  Included by the
+// forward_*.cu units, one per (input, output) pair.
 //
 // Computes, for every interval of the scatter map ("Accelerating BEV Pooling
 // on NVIDIA GPUs for Physical AI Applications", sections "Eliminate redundant
 // scatter traffic" and "Implement interval-owned scatter-reduce"),
 //     out[bev, :] = scale * sum_{t in interval} depth[ranks_depth[t]] * feat[ranks_feat[t], :]
-// in FP32, rounded once to fp16, and writes every other cell as zeros, so
+// in FP32, rounded once to the output type (fp16, or E4M3 codes of
+// value / out_scale), and writes every other cell as zeros, so
 // each output row is written exactly once and no atomics are used.
 //
 // One launch, two kinds of CTA: compute CTAs take the first block indices (the
@@ -46,8 +48,8 @@
 
 #include "bevpool_internal.cuh"
 
-// Launch and inner-loop constants, chosen by measurement on GB300 (the design
-// notes list what else was tried); each can be overridden with -D.
+// Launch and inner-loop constants, each chosen by timing it against
+// alternatives on GB300; each can be overridden with -D.
 #ifndef BEVPOOL_FWD_MIN_CTAS
 #define BEVPOOL_FWD_MIN_CTAS 3            // resident CTAs per SM the register budget (80) is sized for
 #endif

@@ -20,7 +20,7 @@
  *     run of scatter points that share one BEV cell; its owner writes the
  *     cell once.
  *
- * Readings where the pages are silent (each is listed in the design notes):
+ * Readings where the pages are silent:
  *   - frustum point index p = ((nc*D + d)*H + h)*W + w; depth is laid out
  *     [NC, D, H, W] so ranks_depth = p; feat is NHWC [NC, H, W, C] so
  *     ranks_feat = (nc*H + h)*W + w; out is [n_cells, C] row-major;

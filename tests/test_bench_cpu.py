@@ -61,7 +61,8 @@ def test_forward_source_hash_ignores_comments_only(tmp_path, monkeypatch):
 
 
 def test_bytes_model_matches_the_stated_formula():
-    """Footprint and gather bytes of the canonical workload as the design notes state them."""
+    """Footprint and gather bytes of the canonical workload: 12 B per point of ranks, 8 B per interval,
+    the depth and feature tensors, the output (footprint); the per-point depth and row reads (gather)."""
     import importlib.util
 
     spec = importlib.util.spec_from_file_location("bench_under_test2", os.path.join(ROOT, "bench.py"))

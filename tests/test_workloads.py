@@ -1,6 +1,6 @@
 """The seeded workload generators: shapes and the stated point counts (the
-recipes are in the design notes; these counts are what the parity tests and
-the benchmark run on)."""
+recipes are in the generators' docstrings; these counts are what the parity
+tests and the benchmark run on)."""
 import numpy as np
 import pytest
 
