@@ -320,6 +320,6 @@ def test_forward_skips_out_of_range_entries(bp, wl_cache):
     cid[dropped] = -1
     ref = oracle.forward(wl.dtype, cid, *wl.dims(), wl.n_cells, wl.C, wl.depth, wl.feat, wl.depth_scale,
                          wl.feat_scale)
-    assert_forward_close(wl, out, ref)
+    assert_forward_close(wl, out, ref, cell_ids=cid)
     g = out.float().cpu().numpy()
     assert np.all(g[int(h["ranks_bev"][s[0]])] == 0) and np.all(g[int(h["ranks_bev"][s[-1]])] == 0)
