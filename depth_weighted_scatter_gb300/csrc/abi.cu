@@ -125,9 +125,8 @@ inline bevpool_status cuda_status(cudaError_t e) {
 }
 
 inline bool frustum_ok(int32_t NC, int32_t D, int32_t H, int32_t W) {
-    if (NC < 1 || D < 1 || H < 1 || W < 1) return false;
-    const int64_t nf = static_cast<int64_t>(NC) * D * H * W;
-    return nf <= INT32_MAX;
+    int64_t nf = 0;
+    return frustum_points(NC, D, H, W, &nf);
 }
 
 }  // namespace
@@ -149,6 +148,11 @@ const char *bevpool_status_string(bevpool_status status) {
 int32_t bevpool_version(void) { return 200; }   // 0.2.0: E4M3 output, NVFP4 features, per-frame call
 
 int64_t bevpool_kernel_launches(void) { return g_kernel_launches.load(std::memory_order_relaxed); }
+
+int64_t bevpool_forward_wait_timeouts(void) {
+    return static_cast<int64_t>(pipe_wait_timeouts_f16()) + pipe_wait_timeouts_e4m3() +
+           pipe_wait_timeouts_f16_e4m3out() + pipe_wait_timeouts_e4m3_e4m3out();
+}
 
 int32_t bevpool_forward_supported(bevpool_dtype dtype, int32_t C) {
     return forward_supported(static_cast<int>(dtype), C) ? 1 : 0;

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <climits>
 
 #include "../../include/bevpool.h"
 #include "fastdiv.h"
@@ -29,6 +30,20 @@ struct DeviceInfo {
 bool device_info(DeviceInfo *out);
 
 inline int64_t div_up(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Number of frustum points NC*D*H*W into *nf, or false if a factor is below 1
+// or the product exceeds INT32_MAX (checked one multiply at a time, so the
+// product never overflows).
+inline bool frustum_points(int32_t NC, int32_t D, int32_t H, int32_t W, int64_t *nf) {
+    if (NC < 1 || D < 1 || H < 1 || W < 1) return false;
+    int64_t n = NC;
+    for (const int32_t f : {D, H, W}) {
+        if (n > INT32_MAX / f) return false;
+        n *= f;
+    }
+    *nf = n;
+    return true;
+}
 
 // Programmatic dependent launch.  A kernel launched with launch_dependent()
 // may be scheduled while the previous kernel of the stream is still running
@@ -170,6 +185,11 @@ cudaError_t launch_forward_f16_e4m3out(const ForwardArgs &a);     // E4M3 output
 cudaError_t launch_forward_e4m3_e4m3out(const ForwardArgs &a);
 cudaError_t launch_forward_nvfp4(const ForwardArgs &a);           // NVFP4 features, fp16 output
 cudaError_t launch_forward_nvfp4_e4m3out(const ForwardArgs &a);   // NVFP4 features, E4M3 output
+// Timed-out waits of the warp-specialised forward, one counter per compiled unit.
+unsigned int pipe_wait_timeouts_f16();
+unsigned int pipe_wait_timeouts_e4m3();
+unsigned int pipe_wait_timeouts_f16_e4m3out();
+unsigned int pipe_wait_timeouts_e4m3_e4m3out();
 
 // Map validation (abi.cu).
 cudaError_t launch_validate_map(const int32_t *ranks_depth, const int32_t *ranks_feat,

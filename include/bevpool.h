@@ -80,6 +80,13 @@ BEVPOOL_API int32_t bevpool_version(void);
  * (all devices, all streams).  Used to count launches in a timed region. */
 BEVPOOL_API int64_t bevpool_kernel_launches(void);
 
+/* Number of bounded waits inside the forward kernels of the current device
+ * that ran out since the library was loaded (0 in a correct run).  A forward
+ * whose wait ran out stores nothing more from the waiting thread and still
+ * ends, so a nonzero count means its output is incomplete.  Synchronises
+ * with the device; not for use inside stream capture. */
+BEVPOOL_API int64_t bevpool_forward_wait_timeouts(void);
+
 /* Whether channel count C has a compiled forward kernel for dtype (1 / 0);
  * for BEVPOOL_NVFP4 it answers for bevpool_forward_nvfp4. */
 BEVPOOL_API int32_t bevpool_forward_supported(bevpool_dtype dtype, int32_t C);
@@ -145,7 +152,14 @@ BEVPOOL_API bevpool_status bevpool_build_map(const int32_t *cell_ids, int32_t NC
  *     the caller.  Nothing in the array needs clearing between calls.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress), which cannot happen during stream capture: make
- *     the first call on a device outside any capture.
+ *     the first call on a device outside any capture.  A call after
+ *     cudaDeviceReset finds the device's context changed and looks the
+ *     address up again, so the first call after a reset must also be made
+ *     outside any capture.
+ *   - Under lazy module loading (the CUDA default) that first look-up is
+ *     what commits the array's memory on the device, so it is the one call
+ *     that can fail for lack of device memory (BEVPOOL_ERR_CUDA).  Callers
+ *     that must not fail later make one call at start-up.
  */
 #define BEVPOOL_NOALLOC_MAX_FRUSTUM (1 << 21)
 #define BEVPOOL_NOALLOC_SCRATCH_BYTES (37u * 1024u * 1024u)

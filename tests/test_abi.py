@@ -92,12 +92,22 @@ def test_build_map_rejects_bad_arguments(bp):
                 ranks_bev=FAKE, interval_starts=FAKE, interval_lengths=FAKE, d_counts=FAKE, h_counts=h,
                 workspace=FAKE, workspace_bytes=ws, stream=0)
     bad = [dict(NC=0), dict(D=-1), dict(n_cells=0), dict(cell_ids=0), dict(d_counts=0),
-           dict(ranks_feat=FAKE + 2), dict(NC=1 << 16, D=1 << 16)]
+           dict(ranks_feat=FAKE + 2), dict(NC=1 << 16, D=1 << 16),
+           # products that overflow 64 bits when formed in one expression (2^64 wraps to 0)
+           dict(NC=1 << 16, D=1 << 16, H=1 << 16, W=1 << 16), dict(NC=2 ** 31 - 1, D=2 ** 31 - 1, H=2, W=2)]
     for change in bad:
         assert bp.bevpool_build_map(**{**args, **change}) == bp.BEVPOOL_ERR_INVALID_ARG, change
     assert bp.bevpool_build_map(**{**args, "workspace": 0}) == bp.BEVPOOL_ERR_WORKSPACE
     assert bp.bevpool_build_map(**{**args, "workspace_bytes": ws - 1}) == bp.BEVPOOL_ERR_WORKSPACE
     assert bp.bevpool_build_map(**{**args, "workspace": FAKE + 64}) == bp.BEVPOOL_ERR_WORKSPACE
+
+
+def test_build_map_noalloc_rejects_bad_arguments(bp):
+    args = dict(cell_ids=FAKE, NC=2, D=3, H=4, W=5, n_cells=10, ranks_depth=FAKE, ranks_feat=FAKE,
+                ranks_bev=FAKE, interval_starts=FAKE, interval_lengths=FAKE, d_counts=FAKE, h_counts=None, stream=0)
+    for change in [dict(NC=0), dict(n_cells=0), dict(NC=1 << 16, D=1 << 16, H=1 << 16, W=1 << 16)]:
+        assert bp.bevpool_build_map_noalloc(**{**args, **change}) == bp.BEVPOOL_ERR_INVALID_ARG, change
+    assert bp.bevpool_build_map_noalloc(**{**args, "D": 1 << 20}) == bp.BEVPOOL_ERR_WORKSPACE
 
 
 def test_forward_rejects_bad_arguments(bp):
