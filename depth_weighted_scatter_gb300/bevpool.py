@@ -48,8 +48,6 @@ _lib.bevpool_version.argtypes = []
 _lib.bevpool_version.restype = _i32
 _lib.bevpool_kernel_launches.argtypes = []
 _lib.bevpool_kernel_launches.restype = _i64
-_lib.bevpool_forward_wait_timeouts.argtypes = []
-_lib.bevpool_forward_wait_timeouts.restype = _i64
 _lib.bevpool_forward_supported.argtypes = [ctypes.c_int, _i32]
 _lib.bevpool_forward_supported.restype = _i32
 _lib.bevpool_build_map_workspace_size.argtypes = [_i64, _i32]
@@ -98,10 +96,6 @@ def bevpool_version() -> int:
 
 def bevpool_kernel_launches() -> int:
     return _lib.bevpool_kernel_launches()
-
-
-def bevpool_forward_wait_timeouts() -> int:
-    return _lib.bevpool_forward_wait_timeouts()
 
 
 def bevpool_forward_supported(dtype: int, C: int) -> bool:

@@ -149,11 +149,6 @@ int32_t bevpool_version(void) { return 200; }   // 0.2.0: E4M3 output, NVFP4 fea
 
 int64_t bevpool_kernel_launches(void) { return g_kernel_launches.load(std::memory_order_relaxed); }
 
-int64_t bevpool_forward_wait_timeouts(void) {
-    return static_cast<int64_t>(pipe_wait_timeouts_f16()) + pipe_wait_timeouts_e4m3() +
-           pipe_wait_timeouts_f16_e4m3out() + pipe_wait_timeouts_e4m3_e4m3out();
-}
-
 int32_t bevpool_forward_supported(bevpool_dtype dtype, int32_t C) {
     return forward_supported(static_cast<int>(dtype), C) ? 1 : 0;
 }

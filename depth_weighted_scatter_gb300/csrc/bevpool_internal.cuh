@@ -185,11 +185,6 @@ cudaError_t launch_forward_f16_e4m3out(const ForwardArgs &a);     // E4M3 output
 cudaError_t launch_forward_e4m3_e4m3out(const ForwardArgs &a);
 cudaError_t launch_forward_nvfp4(const ForwardArgs &a);           // NVFP4 features, fp16 output
 cudaError_t launch_forward_nvfp4_e4m3out(const ForwardArgs &a);   // NVFP4 features, E4M3 output
-// Timed-out waits of the warp-specialised forward, one counter per compiled unit.
-unsigned int pipe_wait_timeouts_f16();
-unsigned int pipe_wait_timeouts_e4m3();
-unsigned int pipe_wait_timeouts_f16_e4m3out();
-unsigned int pipe_wait_timeouts_e4m3_e4m3out();
 
 // Map validation (abi.cu).
 cudaError_t launch_validate_map(const int32_t *ranks_depth, const int32_t *ranks_feat,

@@ -20,6 +20,4 @@ cudaError_t launch_forward_e4m3(const ForwardArgs &a) {
     }
 }
 
-unsigned int pipe_wait_timeouts_e4m3() { return pipe_wait_timeouts_here(); }
-
 }  // namespace bevpool

@@ -20,6 +20,4 @@ cudaError_t launch_forward_f16(const ForwardArgs &a) {
     }
 }
 
-unsigned int pipe_wait_timeouts_f16() { return pipe_wait_timeouts_here(); }
-
 }  // namespace bevpool

@@ -19,6 +19,4 @@ cudaError_t launch_forward_f16_e4m3out(const ForwardArgs &a) {
     }
 }
 
-unsigned int pipe_wait_timeouts_f16_e4m3out() { return pipe_wait_timeouts_here(); }
-
 }  // namespace bevpool

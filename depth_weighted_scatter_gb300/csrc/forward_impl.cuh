@@ -107,9 +107,6 @@
 // Compute CTAs per SM (one wave of them): with the output resident in L2,
 // two, leaving a slot for fill CTAs to run alongside; when the output streams
 // to DRAM, three (the gathers need the issue slots more than the fills).
-#ifndef BEVPOOL_FWD_PIPE
-#define BEVPOOL_FWD_PIPE 0                // 1: the warp-specialised forward where it applies (forward_pipe.cuh)
-#endif
 #ifndef BEVPOOL_FWD_CTAS_PER_SM_L2
 #define BEVPOOL_FWD_CTAS_PER_SM_L2 2
 #endif
@@ -947,11 +944,6 @@ cudaError_t launch_forward_v(const ForwardArgs &a) {
     return e;
 }
 
-}  // namespace bevpool
-
-#include "forward_pipe.cuh"
-
-namespace bevpool {
 
 // fp16 rows take the lean variant when the output streams to DRAM (measured:
 // DRAM batch 122.9 -> 114.7 us) and when there is much work per SM even with
@@ -966,9 +958,6 @@ namespace bevpool {
 // 1.28M points 39.4 -> 41.0, C = 128 13.7 -> 14.0).
 template <int DT, int C, int OT>
 cudaError_t launch_forward_t(const ForwardArgs &a) {
-#if BEVPOOL_FWD_PIPE
-    if constexpr (pipe_supported<DT, C>()) return launch_forward_pipe<DT, C, OT>(a);
-#endif
     if constexpr (DT == kDtypeE4M3) {
         if (a.streaming_stores) return launch_forward_v<DT, C, OT, kVarLean>(a);
     }

@@ -80,13 +80,6 @@ BEVPOOL_API int32_t bevpool_version(void);
  * (all devices, all streams).  Used to count launches in a timed region. */
 BEVPOOL_API int64_t bevpool_kernel_launches(void);
 
-/* Number of bounded waits inside the forward kernels of the current device
- * that ran out since the library was loaded (0 in a correct run).  A forward
- * whose wait ran out stores nothing more from the waiting thread and still
- * ends, so a nonzero count means its output is incomplete.  Synchronises
- * with the device; not for use inside stream capture. */
-BEVPOOL_API int64_t bevpool_forward_wait_timeouts(void);
-
 /* Whether channel count C has a compiled forward kernel for dtype (1 / 0);
  * for BEVPOOL_NVFP4 it answers for bevpool_forward_nvfp4. */
 BEVPOOL_API int32_t bevpool_forward_supported(bevpool_dtype dtype, int32_t C);

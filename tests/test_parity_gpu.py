@@ -324,8 +324,3 @@ def test_forward_skips_out_of_range_entries(bp, wl_cache):
     g = out.float().cpu().numpy()
     assert np.all(g[int(h["ranks_bev"][s[0]])] == 0) and np.all(g[int(h["ranks_bev"][s[-1]])] == 0)
 
-
-def test_no_forward_wait_ran_out(bp):
-    """Every bounded wait of the forward kernels run so far in this process
-    completed (a wait that runs out leaves its rows unwritten)."""
-    assert bp.bevpool_forward_wait_timeouts() == 0
