@@ -26,6 +26,9 @@ def test_reference_arm_json_line():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["cpu_baseline"]["cpu_model"] and d["cpu_baseline"]["median"] > 0
     assert "workload" in d["config"]
+    # the oracle runs on the host: its line claims no GPU-side timing conditions, and keeps the given warm-up
+    assert "l2" not in d["config"] and "parallelism" not in d["config"] and "host" in d["config"]
+    assert d["warmup"] == 1 and d["steps"] == 2
 
 
 def test_reference_arm_e4m3_output_and_nvfp4():
