@@ -50,6 +50,9 @@ _lib.bevpool_kernel_launches.argtypes = []
 _lib.bevpool_kernel_launches.restype = _i64
 _lib.bevpool_forward_supported.argtypes = [ctypes.c_int, _i32]
 _lib.bevpool_forward_supported.restype = _i32
+_lib.bevpool_forward_plan.argtypes = [ctypes.c_int, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                      _i64, _vp]
+_lib.bevpool_forward_plan.restype = ctypes.c_int
 _lib.bevpool_build_map_workspace_size.argtypes = [_i64, _i32]
 _lib.bevpool_build_map_workspace_size.restype = _sz
 _lib.bevpool_build_map.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
@@ -100,6 +103,30 @@ def bevpool_kernel_launches() -> int:
 
 def bevpool_forward_supported(dtype: int, C: int) -> bool:
     return bool(_lib.bevpool_forward_supported(dtype, C))
+
+
+PLAN_FIELDS = ("variant", "ctas_per_sm", "owners", "batch", "round", "n_compute", "fill_cells", "n_fill",
+               "streaming")
+
+
+def bevpool_forward_plan(dtype: int, C: int, e4m3_out: int, NC: int, D: int, H: int, W: int, n_points: int,
+                         n_intervals: int, counts_on_device: int, n_cells: int, sm_count: int, l2_bytes: int,
+                         plan: np.ndarray) -> int:
+    return _lib.bevpool_forward_plan(dtype, C, e4m3_out, NC, D, H, W, n_points, n_intervals, counts_on_device,
+                                     n_cells, sm_count, l2_bytes, _host_ptr(plan))
+
+
+def forward_plan(dtype: int, C: int, NC: int, D: int, H: int, W: int, n_points: int, n_intervals: int,
+                 n_cells: int, *, e4m3_out: bool = False, counts_on_device: bool = False, sm_count: int = 0,
+                 l2_bytes: int = 0) -> dict:
+    """The launch plan of a forward call with these sizes, as a dict of
+    PLAN_FIELDS (sm_count and l2_bytes > 0: for that GPU, without one)."""
+    plan = np.zeros(len(PLAN_FIELDS), dtype=np.int32)
+    st = bevpool_forward_plan(dtype, C, int(e4m3_out), NC, D, H, W, n_points, n_intervals, int(counts_on_device),
+                              n_cells, sm_count, l2_bytes, plan)
+    if st != BEVPOOL_OK:
+        raise BevpoolError(st, "bevpool_forward_plan")
+    return dict(zip(PLAN_FIELDS, (int(x) for x in plan)))
 
 
 def bevpool_build_map_workspace_size(n_frustum: int, n_cells: int) -> int:

@@ -205,8 +205,60 @@ bevpool_status bevpool_build_map(const int32_t *cell_ids, int32_t NC, int32_t D,
 
 namespace {
 
-// Shared body of the two forward entry points (fp16 output, or E4M3 output
-// codes of value / out_scale).
+// The size checks of a forward call (no device needed).
+bevpool_status forward_sizes_ok(bevpool_dtype dtype, int32_t NC, int32_t D, int32_t H, int32_t W, int32_t C,
+                                bool e4m3_out, int32_t n_points, int32_t n_intervals, int32_t n_cells) {
+    if (dtype != BEVPOOL_F16 && dtype != BEVPOOL_E4M3 && dtype != BEVPOOL_NVFP4) return BEVPOOL_ERR_UNSUPPORTED;
+    if (!forward_supported(static_cast<int>(dtype), C)) return BEVPOOL_ERR_UNSUPPORTED;
+    if (e4m3_out && C % 16 != 0) return BEVPOOL_ERR_UNSUPPORTED;
+    if (!frustum_ok(NC, D, H, W) || n_cells < 1) return BEVPOOL_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(n_cells) * C > INT32_MAX) return BEVPOOL_ERR_INVALID_ARG;
+    const int64_t nf = static_cast<int64_t>(NC) * D * H * W;
+    if (n_points < 0 || n_intervals < 0 || n_points > nf || n_intervals > n_points) return BEVPOOL_ERR_INVALID_ARG;
+    return BEVPOOL_OK;
+}
+
+// The size checks and launch-shaping choices of a forward call, without its
+// pointers: fills every size field of *a, the memory regime and the SM count.
+bevpool_status forward_prepare(bevpool_dtype dtype, int32_t NC, int32_t D, int32_t H, int32_t W, int32_t C,
+                               bool e4m3_out, int32_t n_points, int32_t n_intervals, bool counts_on_device,
+                               int32_t n_cells, const DeviceInfo &info, ForwardArgs *a) {
+    const bevpool_status st = forward_sizes_ok(dtype, NC, D, H, W, C, e4m3_out, n_points, n_intervals, n_cells);
+    if (st != BEVPOOL_OK) return st;
+    const int64_t nf = static_cast<int64_t>(NC) * D * H * W;
+    *a = ForwardArgs{};
+    a->n_points = n_points;
+    a->n_intervals = n_intervals;
+    a->n_cells = n_cells;
+    a->C = C;
+    a->n_depth = nf;
+    a->n_feat_rows = NC * H * W;
+    a->out_e4m3 = e4m3_out ? 1 : 0;
+    // Memory regime (section "Classify the memory regime"): when the bytes the
+    // forward touches do not fit comfortably in L2, stream the output past it.
+    const int64_t eb = dtype == BEVPOOL_F16 ? 2 : 1;
+    const int64_t ob = e4m3_out ? 1 : 2;
+    const int64_t feat_bytes = dtype == BEVPOOL_NVFP4 ? static_cast<int64_t>(a->n_feat_rows) * (C / 2 + C / 16)
+                                                      : static_cast<int64_t>(a->n_feat_rows) * C * eb;
+    const int64_t footprint = static_cast<int64_t>(n_points) * 12 + static_cast<int64_t>(n_intervals) * 8 +
+                              nf * eb + feat_bytes + static_cast<int64_t>(n_cells) * C * ob;
+    a->streaming_stores = footprint > static_cast<int64_t>(info.l2_bytes) / 2 ? 1 : 0;
+    // Device counts bounded by the whole frustum (what bevpool_pool_frame
+    // passes) say nothing about the actual count: size the launch for one
+    // resident wave and leave the choice of variant to the memory regime.
+    a->loose_capacity = counts_on_device && n_points >= nf ? 1 : 0;
+    a->sm_count = info.sm_count;
+    return BEVPOOL_OK;
+}
+
+cudaError_t forward_dispatch(bevpool_dtype dtype, bool e4m3_out, const ForwardArgs &a) {
+    if (dtype == BEVPOOL_NVFP4) return e4m3_out ? launch_forward_nvfp4_e4m3out(a) : launch_forward_nvfp4(a);
+    if (e4m3_out) return dtype == BEVPOOL_F16 ? launch_forward_f16_e4m3out(a) : launch_forward_e4m3_e4m3out(a);
+    return dtype == BEVPOOL_F16 ? launch_forward_f16(a) : launch_forward_e4m3(a);
+}
+
+// Shared body of the forward entry points (fp16 output, or E4M3 output codes
+// of value / out_scale).
 bevpool_status forward_impl(bevpool_dtype dtype, const void *depth, const void *feat, const void *feat_block,
                             int32_t NC, int32_t D, int32_t H, int32_t W, int32_t C, float depth_scale,
                             float feat_scale, bool e4m3_out,
@@ -214,14 +266,9 @@ bevpool_status forward_impl(bevpool_dtype dtype, const void *depth, const void *
                             const int32_t *ranks_bev, const int32_t *interval_starts,
                             const int32_t *interval_lengths, int32_t n_points, int32_t n_intervals,
                             const int32_t *d_counts, int32_t n_cells, void *out, void *stream) {
-    if (dtype != BEVPOOL_F16 && dtype != BEVPOOL_E4M3 && dtype != BEVPOOL_NVFP4) return BEVPOOL_ERR_UNSUPPORTED;
-    if (!forward_supported(static_cast<int>(dtype), C)) return BEVPOOL_ERR_UNSUPPORTED;
-    if (e4m3_out && C % 16 != 0) return BEVPOOL_ERR_UNSUPPORTED;
+    const bevpool_status sz = forward_sizes_ok(dtype, NC, D, H, W, C, e4m3_out, n_points, n_intervals, n_cells);
+    if (sz != BEVPOOL_OK) return sz;
     if (dtype == BEVPOOL_NVFP4 && !feat_block) return BEVPOOL_ERR_INVALID_ARG;
-    if (!frustum_ok(NC, D, H, W) || n_cells < 1) return BEVPOOL_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(n_cells) * C > INT32_MAX) return BEVPOOL_ERR_INVALID_ARG;
-    const int64_t nf = static_cast<int64_t>(NC) * D * H * W;
-    if (n_points < 0 || n_intervals < 0 || n_points > nf || n_intervals > n_points) return BEVPOOL_ERR_INVALID_ARG;
     if (!depth || !feat || !out) return BEVPOOL_ERR_INVALID_ARG;
     if (n_points > 0 && (!ranks_depth || !ranks_feat || !ranks_bev)) return BEVPOOL_ERR_INVALID_ARG;
     if (n_intervals > 0 && (!interval_starts || !interval_lengths)) return BEVPOOL_ERR_INVALID_ARG;
@@ -237,8 +284,10 @@ bevpool_status forward_impl(bevpool_dtype dtype, const void *depth, const void *
 
     DeviceInfo info;
     if (!device_info(&info)) return BEVPOOL_ERR_CUDA;
-
     ForwardArgs a;
+    const bevpool_status st = forward_prepare(dtype, NC, D, H, W, C, e4m3_out, n_points, n_intervals,
+                                              d_counts != nullptr, n_cells, info, &a);
+    if (st != BEVPOOL_OK) return st;
     a.depth = depth;
     a.feat = feat;
     a.feat_block = feat_block;
@@ -248,38 +297,11 @@ bevpool_status forward_impl(bevpool_dtype dtype, const void *depth, const void *
     a.interval_starts = interval_starts;
     a.interval_lengths = interval_lengths;
     a.d_counts = d_counts;
-    a.n_points = n_points;
-    a.n_intervals = n_intervals;
-    a.n_cells = n_cells;
-    a.C = C;
-    a.n_depth = nf;
-    a.n_feat_rows = NC * H * W;
     a.scale = scale;
-    a.out_e4m3 = e4m3_out ? 1 : 0;
-    // Memory regime (section "Classify the memory regime"): when the bytes the
-    // forward touches do not fit comfortably in L2, stream the output past it.
-    const int64_t eb = dtype == BEVPOOL_F16 ? 2 : 1;
-    const int64_t ob = e4m3_out ? 1 : 2;
-    const int64_t feat_bytes = dtype == BEVPOOL_NVFP4 ? static_cast<int64_t>(a.n_feat_rows) * (C / 2 + C / 16)
-                                                      : static_cast<int64_t>(a.n_feat_rows) * C * eb;
-    const int64_t footprint = static_cast<int64_t>(n_points) * 12 + static_cast<int64_t>(n_intervals) * 8 +
-                              nf * eb + feat_bytes + static_cast<int64_t>(n_cells) * C * ob;
-    a.streaming_stores = footprint > static_cast<int64_t>(info.l2_bytes) / 2 ? 1 : 0;
-    // Device counts bounded by the whole frustum (what bevpool_pool_frame
-    // passes) say nothing about the actual count: size the launch for one
-    // resident wave and leave the choice of variant to the memory regime.
-    a.loose_capacity = d_counts && n_points >= nf ? 1 : 0;
-    a.sm_count = info.sm_count;
     a.out = out;
     a.stream = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (dtype == BEVPOOL_NVFP4)
-        e = e4m3_out ? launch_forward_nvfp4_e4m3out(a) : launch_forward_nvfp4(a);
-    else if (e4m3_out)
-        e = dtype == BEVPOOL_F16 ? launch_forward_f16_e4m3out(a) : launch_forward_e4m3_e4m3out(a);
-    else
-        e = dtype == BEVPOOL_F16 ? launch_forward_f16(a) : launch_forward_e4m3(a);
-    return cuda_status(e);
+    a.plan_out = nullptr;
+    return cuda_status(forward_dispatch(dtype, e4m3_out, a));
 }
 
 }  // namespace
@@ -321,6 +343,35 @@ bevpool_status bevpool_forward_nvfp4(const void *depth, const void *feat, const 
     return forward_impl(BEVPOOL_NVFP4, depth, feat, feat_block, NC, D, H, W, C, depth_scale, feat_scale,
                         out_dtype == BEVPOOL_E4M3, out_scale, ranks_depth, ranks_feat, ranks_bev, interval_starts,
                         interval_lengths, n_points, n_intervals, d_counts, n_cells, out, stream);
+}
+
+bevpool_status bevpool_forward_plan(bevpool_dtype dtype, int32_t C, int32_t e4m3_out, int32_t NC, int32_t D,
+                                    int32_t H, int32_t W, int32_t n_points, int32_t n_intervals,
+                                    int32_t counts_on_device, int32_t n_cells, int32_t sm_count, int64_t l2_bytes,
+                                    int32_t *plan) {
+    if (!plan) return BEVPOOL_ERR_INVALID_ARG;
+    const bevpool_status sz = forward_sizes_ok(dtype, NC, D, H, W, C, e4m3_out != 0, n_points, n_intervals, n_cells);
+    if (sz != BEVPOOL_OK) return sz;
+    DeviceInfo info;
+    if (sm_count > 0 && l2_bytes > 0) {
+        if (l2_bytes > INT32_MAX) return BEVPOOL_ERR_INVALID_ARG;
+        info.sm_count = sm_count;
+        info.l2_bytes = static_cast<int>(l2_bytes);
+    } else if (!device_info(&info)) {
+        return BEVPOOL_ERR_CUDA;
+    }
+    ForwardArgs a;
+    const bevpool_status st = forward_prepare(dtype, NC, D, H, W, C, e4m3_out != 0, n_points, n_intervals,
+                                              counts_on_device != 0, n_cells, info, &a);
+    if (st != BEVPOOL_OK) return st;
+    ForwardPlan pl;
+    a.plan_out = &pl;
+    const bevpool_status ds = cuda_status(forward_dispatch(dtype, e4m3_out != 0, a));
+    if (ds != BEVPOOL_OK) return ds;
+    const int32_t fields[] = {pl.variant, pl.ctas_per_sm, pl.owners, pl.batch, pl.round, pl.n_compute,
+                              pl.fill_cells, pl.n_fill, a.streaming_stores};
+    for (int k = 0; k < 9; ++k) plan[k] = fields[k];
+    return BEVPOOL_OK;
 }
 
 bevpool_status bevpool_pool_frame(const int32_t *cell_ids, int32_t NC, int32_t D, int32_t H, int32_t W,

@@ -160,6 +160,19 @@ cudaError_t launch_build_map(const BuildMapArgs &a);
 cudaError_t launch_build_map_radix(const BuildMapArgs &a);
 cudaError_t launch_build_map_counting(const BuildMapArgs &a);
 
+// The launch plan of one forward call, chosen on the host from the sizes and
+// the device (forward_impl.cuh: plan_variant, launch_forward_t).
+struct ForwardPlan {
+    int32_t variant;          // kernel variant: 0 default, 1 lean, 2 short, 3 lean-short
+    int32_t ctas_per_sm;      // compute CTAs per SM in one wave
+    int32_t owners;           // owners per compute CTA
+    int32_t batch;            // points in flight per owner
+    int32_t round;            // points per staged round of a compute CTA
+    int32_t n_compute;        // compute CTAs
+    int32_t fill_cells;       // cells per fill CTA
+    int32_t n_fill;           // fill CTAs
+};
+
 // Forward (forward_f16.cu / forward_e4m3.cu).
 struct ForwardArgs {
     const void *depth, *feat;
@@ -177,6 +190,7 @@ struct ForwardArgs {
     int sm_count;             // SMs of the current device (launch sizing)
     void *out;
     cudaStream_t stream;
+    ForwardPlan *plan_out;    // non-null: write the launch plan here and launch nothing
 };
 bool forward_supported(int dtype, int C);
 cudaError_t launch_forward_f16(const ForwardArgs &a);             // fp16 output

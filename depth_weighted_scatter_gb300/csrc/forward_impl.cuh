@@ -917,10 +917,50 @@ __global__ void __launch_bounds__(kThreads, FwdShape<DT, C, VAR>::LEAN ? BEVPOOL
         fill_cta<DT, C, OT>(p, idx, sm.f);
 }
 
+// The compute-CTA count and fill tiling of variant VAR for the call's sizes
+// (host code; the launch and bevpool_forward_plan both use it).
+template <int DT, int C, int VAR>
+ForwardPlan plan_variant(const ForwardArgs &a) {
+    using S = FwdShape<DT, C, VAR>;
+    ForwardPlan pl;
+    pl.variant = VAR;
+    pl.ctas_per_sm = S::LEAN ? BEVPOOL_FWD_LEAN_MIN_CTAS
+                             : (a.streaming_stores ? BEVPOOL_FWD_CTAS_PER_SM_DRAM : BEVPOOL_FWD_CTAS_PER_SM_L2);
+    pl.owners = S::OWNERS;
+    pl.batch = S::BATCH;
+    pl.round = ComputeSmem<DT, C, VAR>::ROUND;
+    const int64_t sms = a.sm_count > 0 ? a.sm_count : 148;
+    // About one resident wave of compute CTAs, each with at least a batch of
+    // points per owner; the points per CTA are set on the device from the
+    // actual count.
+    const int64_t slots = sms * pl.ctas_per_sm;
+    int64_t n_compute = div_up(a.n_points, static_cast<int64_t>(S::OWNERS) * S::BATCH);
+    if (n_compute > slots) n_compute = slots;
+#if BEVPOOL_FWD_MULTIWAVE
+    if (!a.loose_capacity) {
+        const int64_t per_cta = pl.round - BEVPOOL_FWD_MULTIWAVE;   // one round each
+        const int64_t want = div_up(a.n_points, per_cta);
+        if (want > n_compute) n_compute = slots * div_up(want, slots);   // whole waves
+    }
+#endif
+    if (n_compute < 1) n_compute = 1;
+    pl.n_compute = static_cast<int32_t>(n_compute);
+    // Fill tiles: about four fill CTAs per SM (each costs a dependent search
+    // before its stores, so large grids take larger tiles).
+    int fill_cells = kFillCellsMin;
+    while (fill_cells < kFillCellsMax && a.n_cells > static_cast<int64_t>(fill_cells) * 4 * sms) fill_cells *= 2;
+    pl.fill_cells = fill_cells;
+    pl.n_fill = static_cast<int32_t>(div_up(a.n_cells, fill_cells));
+    return pl;
+}
+
 template <int DT, int C, int OT, int VAR>
 cudaError_t launch_forward_v(const ForwardArgs &a) {
-    using S = FwdShape<DT, C, VAR>;
-    constexpr bool LEAN = S::LEAN;
+    const ForwardPlan pl = plan_variant<DT, C, VAR>(a);
+    if (a.plan_out) {
+        *a.plan_out = pl;
+        return cudaSuccess;
+    }
     FwdParams p;
     p.depth = a.depth;
     p.feat = a.feat;
@@ -938,38 +978,16 @@ cudaError_t launch_forward_v(const ForwardArgs &a) {
     p.n_depth = a.n_depth;
     p.scale = a.scale;
     p.streaming = a.streaming_stores;
-    // About one resident wave of compute CTAs, each with at least a batch of
-    // points per owner; the points per CTA are set on the device from the
-    // actual count.
-    const int64_t slots = static_cast<int64_t>(a.sm_count > 0 ? a.sm_count : 148) *
-                          (LEAN ? BEVPOOL_FWD_LEAN_MIN_CTAS
-                           : (a.streaming_stores ? BEVPOOL_FWD_CTAS_PER_SM_DRAM : BEVPOOL_FWD_CTAS_PER_SM_L2));
-    int64_t n_compute = div_up(a.n_points, static_cast<int64_t>(S::OWNERS) * S::BATCH);
-    if (n_compute > slots) n_compute = slots;
-#if BEVPOOL_FWD_MULTIWAVE
-    if (!a.loose_capacity) {
-        const int64_t per_cta = ComputeSmem<DT, C, VAR>::ROUND - BEVPOOL_FWD_MULTIWAVE;   // one round each
-        const int64_t want = div_up(a.n_points, per_cta);
-        if (want > n_compute) n_compute = slots * div_up(want, slots);   // whole waves
-    }
-#endif
-    if (n_compute < 1) n_compute = 1;
-    p.n_compute = static_cast<int>(n_compute);
-    p.n_compute_div = FastDiv(static_cast<uint32_t>(n_compute));
-    // Fill tiles: about four fill CTAs per SM (each costs a dependent search
-    // before its stores, so large grids take larger tiles).
-    int fill_cells = kFillCellsMin;
-    const int64_t sms = a.sm_count > 0 ? a.sm_count : 148;
-    while (fill_cells < kFillCellsMax && a.n_cells > static_cast<int64_t>(fill_cells) * 4 * sms) fill_cells *= 2;
-    p.fill_cells = fill_cells;
-    p.n_fill = static_cast<int>(div_up(a.n_cells, fill_cells));
+    p.n_compute = pl.n_compute;
+    p.n_compute_div = FastDiv(static_cast<uint32_t>(pl.n_compute));
+    p.fill_cells = pl.fill_cells;
+    p.n_fill = pl.n_fill;
     p.out = static_cast<unsigned char *>(a.out);
     const int grid = p.n_compute + p.n_fill;
     const cudaError_t e = launch_dependent(k_forward<DT, C, OT, VAR>, dim3(grid), dim3(kThreads), 0, a.stream, p);
     count_launch();
     return e;
 }
-
 
 // fp16 rows take the lean variant when the output streams to DRAM (measured:
 // DRAM batch 122.9 -> 114.7 us) and when there is much work per SM even with

@@ -84,6 +84,36 @@ BEVPOOL_API int64_t bevpool_kernel_launches(void);
  * for BEVPOOL_NVFP4 it answers for bevpool_forward_nvfp4. */
 BEVPOOL_API int32_t bevpool_forward_supported(bevpool_dtype dtype, int32_t C);
 
+/* The launch plan a forward call with these sizes would use (no kernel is
+ * launched and no pointer is needed).  The plan is the library's own launch
+ * shaping, not a step of the pages' method; it is exported so that its rules
+ * can be checked without a GPU.
+ *   dtype, C, e4m3_out  as for bevpool_forward (e4m3_out != 0:
+ *                       bevpool_forward_e4m3_out; BEVPOOL_NVFP4 stands for
+ *                       bevpool_forward_nvfp4);
+ *   NC, D, H, W,
+ *   n_points,
+ *   n_intervals,
+ *   n_cells             as for bevpool_forward;
+ *   counts_on_device    non-zero when the call passes d_counts (then n_points
+ *                       and n_intervals are capacities);
+ *   sm_count, l2_bytes  the GPU to plan for; when either is <= 0, the current
+ *                       device (which then needs a GPU);
+ *   plan                host int32[9], filled with {variant (0 default,
+ *                       1 lean, 2 short intervals, 3 lean with short
+ *                       intervals), compute CTAs per SM, owners per compute
+ *                       CTA, points in flight per owner, points per staged
+ *                       round, compute CTAs, cells per fill CTA, fill CTAs,
+ *                       streaming output stores (1: the output is written
+ *                       past the L2)}.
+ * Returns what bevpool_forward would for the same sizes
+ * (BEVPOOL_ERR_UNSUPPORTED / BEVPOOL_ERR_INVALID_ARG), BEVPOOL_ERR_INVALID_ARG
+ * for a null plan. */
+BEVPOOL_API bevpool_status bevpool_forward_plan(bevpool_dtype dtype, int32_t C, int32_t e4m3_out, int32_t NC,
+                                                int32_t D, int32_t H, int32_t W, int32_t n_points,
+                                                int32_t n_intervals, int32_t counts_on_device, int32_t n_cells,
+                                                int32_t sm_count, int64_t l2_bytes, int32_t *plan);
+
 /*
  * Bytes of device workspace bevpool_build_map needs for a frustum of
  * n_frustum = NC*D*H*W points and a grid of n_cells cells.  Returns 0 for
