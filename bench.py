@@ -88,16 +88,17 @@ def measured_peaks() -> tuple:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per forward launch from a committed ncu capture, if it was
-    taken on the current forward source."""
+def recorded_traffic(workload: str, key: str = "dram_bytes_per_launch"):
+    """Bytes per forward launch from a committed ncu capture (DRAM bytes with
+    caches flushed, or with key="l2_bytes_warm" the L2 bytes of a warm
+    launch), if it was taken on the current forward source."""
     p = os.path.join(ROOT, "profiles", "forward_traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
         e = d.get(workload)
-        if e and e.get("source_hash") == forward_source_hash():
-            return float(e["dram_bytes_per_launch"])
+        if e and e.get("source_hash") == forward_source_hash() and key in e:
+            return float(e[key])
     except Exception:
         pass
     return None
@@ -696,6 +697,8 @@ def run_ours(args) -> None:
                 "peak_source": f"hbm_gbs of MEASURED_PEAKS.json ({peak_kind})"}
     if roof_l2 is not None:
         roof_l2["traffic"] = roof_hbm["traffic"]
+        roof_l2["traffic_note"] = "DRAM bytes of one launch with caches flushed (ncu); l2_traffic: L2 bytes of a warm launch"
+        roof_l2["l2_traffic"] = recorded_traffic(traffic_key, "l2_bytes_warm")
     line = {
         "metric": METRIC,
         "value": fwd_mean * 1e3,

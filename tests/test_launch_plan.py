@@ -29,10 +29,18 @@ def footprint(dtype, C, n_points, n_intervals, n_cells, dims=CANON, e4m3_out=Fal
     return 12 * n_points + 8 * n_intervals + nf * eb + feat + n_cells * C * (1 if e4m3_out else 2)
 
 
-def expected_fill_cells(n_cells, sms=SMS):
-    f = 256
-    while f < 1024 and n_cells > f * 4 * sms:
-        f *= 2
+def expected_fill_cells(n_cells, n_points, row_bytes, streaming, sms=SMS):
+    """Output in L2: the largest power of two in [128, 1024] with at most 80 KB
+    of rows, at most 1024 points on average and at least one tile per SM.
+    Streaming: 256 doubled while the grid exceeds four tiles per SM, at most 1024."""
+    if streaming:
+        f = 256
+        while f < 1024 and n_cells > f * 4 * sms:
+            f *= 2
+        return f
+    f = 1024
+    while f > 128 and (f * row_bytes > 80 * 1024 or n_points * f > 1024 * n_cells or -(-n_cells // f) < sms):
+        f //= 2
     return f
 
 
@@ -42,16 +50,16 @@ def test_plans_of_the_five_configurations():
     """The plans the benchmarked workloads get (regression pins of the rules below)."""
     canon = plan(bp.BEVPOOL_F16, 80, 209_077, 57_403, 129_600)
     assert (canon["variant"], canon["ctas_per_sm"], canon["n_compute"], canon["fill_cells"], canon["n_fill"],
-            canon["streaming"]) == (SHORT, 2, 304, 256, 507, 0)
+            canon["streaming"]) == (SHORT, 2, 304, 512, 254, 0)
     fp8 = plan(bp.BEVPOOL_E4M3, 80, 209_077, 57_403, 129_600)
     assert (fp8["variant"], fp8["n_compute"], fp8["streaming"]) == (DEFAULT, 304, 0)
     bevdet = plan(bp.BEVPOOL_F16, 64, 182_660, 9_452, 16_384, dims=dict(NC=6, D=59, H=16, W=44))
-    assert (bevdet["variant"], bevdet["n_compute"], bevdet["n_fill"]) == (DEFAULT, 304, 64)
+    assert (bevdet["variant"], bevdet["n_compute"], bevdet["fill_cells"], bevdet["n_fill"]) == (DEFAULT, 304, 128, 128)
     dram = plan(bp.BEVPOOL_F16, 128, 2_198_618, 738_763, 1 << 20, dims=dict(NC=24, D=118, H=32, W=88))
     assert (dram["variant"], dram["ctas_per_sm"], dram["n_compute"], dram["fill_cells"], dram["n_fill"],
             dram["streaming"]) == (LEAN_SHORT, 4, 2432, 1024, 1024, 1)
     tiny = plan(bp.BEVPOOL_F16, 8, 190, 150, 256, dims=dict(NC=1, D=8, H=4, W=8))
-    assert tiny["n_compute"] == 1 and tiny["n_fill"] == 1 and tiny["streaming"] == 0
+    assert tiny["n_compute"] == 1 and tiny["n_fill"] == 2 and tiny["streaming"] == 0
 
 
 # ------------------------------------------------------------------ variant rules
@@ -160,19 +168,29 @@ def test_rounds_fit_the_shared_memory_of_wide_rows():
 
 @pytest.mark.parametrize("n_cells", [1, 255, 256, 4_096, 16_384, 129_600, 155_648, 155_649, 311_296, 311_297,
                                      1 << 20, 4 << 20])
-def test_fill_tiles_double_with_the_grid(n_cells):
-    """Cells per fill CTA: 256, doubled while the grid exceeds four tiles per
-    SM, at most 1024; the fill CTAs cover the grid exactly once."""
-    C = 8 if n_cells > (1 << 20) else 80
-    p = plan(bp.BEVPOOL_F16, C, 100, 50, n_cells)
-    assert p["fill_cells"] == expected_fill_cells(n_cells)
-    assert p["n_fill"] == -(-n_cells // p["fill_cells"])
-    assert (p["n_fill"] - 1) * p["fill_cells"] < n_cells <= p["n_fill"] * p["fill_cells"]
+@pytest.mark.parametrize("points_per_cell", [0.01, 1.6, 8.0, 11.0])
+def test_fill_tiles(n_cells, points_per_cell):
+    """Cells per fill CTA by the two rules (the output in L2 or streaming past
+    it); the fill CTAs cover the grid exactly once."""
+    dims = dict(NC=96, D=118, H=32, W=88)                       # room for every point count below
+    for C in (8, 80, 256):
+        if n_cells * C >= 1 << 31:
+            continue
+        n = min(int(n_cells * points_per_cell), 96 * 118 * 32 * 88)
+        p = plan(bp.BEVPOOL_F16, C, n, max(0, min(n, n_cells) // 2), n_cells, dims=dims)
+        assert p["fill_cells"] == expected_fill_cells(n_cells, n, 2 * C, p["streaming"] == 1), (n_cells, n, C, p)
+        assert p["n_fill"] == -(-n_cells // p["fill_cells"])
+        assert (p["n_fill"] - 1) * p["fill_cells"] < n_cells <= p["n_fill"] * p["fill_cells"]
 
 
-def test_fill_tiles_follow_the_sm_count():
+def test_fill_tiles_follow_the_sm_count_and_the_regime():
+    # output in L2: at least one fill CTA per SM
     assert plan(bp.BEVPOOL_F16, 80, 100, 50, 200_000, sms=152)["fill_cells"] == 512
-    assert plan(bp.BEVPOOL_F16, 80, 100, 50, 200_000, sms=256)["fill_cells"] == 256
+    assert plan(bp.BEVPOOL_F16, 80, 100, 50, 200_000, sms=256)["fill_cells"] == 512
+    assert plan(bp.BEVPOOL_F16, 80, 100, 50, 100_000, sms=256)["fill_cells"] == 256
+    # streaming: four fill CTAs per SM
+    assert plan(bp.BEVPOOL_F16, 80, 100, 50, 200_000, sms=152, l2=1 << 20)["fill_cells"] == 512
+    assert plan(bp.BEVPOOL_F16, 80, 100, 50, 200_000, sms=256, l2=1 << 20)["fill_cells"] == 256
 
 
 # ------------------------------------------------------------------ refusals
