@@ -57,10 +57,13 @@
 #define BEVPOOL_FWD_LANE_BYTES 16         // bytes of an fp16 feature row one lane loads (16 or 32)
 #endif
 #ifndef BEVPOOL_FWD_E4M3_LANE_BYTES
-#define BEVPOOL_FWD_E4M3_LANE_BYTES 16    // bytes of an E4M3 feature row one lane loads
+#define BEVPOOL_FWD_E4M3_LANE_BYTES 8     // bytes of an E4M3 feature row one lane loads
 #endif
 #ifndef BEVPOOL_FWD_BATCH
-#define BEVPOOL_FWD_BATCH 6               // points in flight per owner: fp16 rows, and E4M3 rows under 16 B a lane
+#define BEVPOOL_FWD_BATCH 6               // points in flight per owner: fp16 rows
+#endif
+#ifndef BEVPOOL_FWD_E4M3_BATCH8
+#define BEVPOOL_FWD_E4M3_BATCH8 6         // E4M3 rows at 8 B or less a lane
 #endif
 #ifndef BEVPOOL_FWD_E4M3_BATCH16
 #define BEVPOOL_FWD_E4M3_BATCH16 5        // E4M3 rows at 16 B a lane (5 rows of 16 B beside 16 FP32 sums)
@@ -90,7 +93,7 @@
 #define BEVPOOL_FWD_PIPELINE 0            // > 0: fp16 owners walk in a two-stage pipeline of this many points
 #endif
 #ifndef BEVPOOL_FWD_PIPELINE_FP8
-#define BEVPOOL_FWD_PIPELINE_FP8 2        // the same for E4M3 rows
+#define BEVPOOL_FWD_PIPELINE_FP8 0        // the same for E4M3 rows
 #endif
 #ifndef BEVPOOL_FWD_PIPELINE_NVFP4
 #define BEVPOOL_FWD_PIPELINE_NVFP4 2      // the same for NVFP4 rows
@@ -107,8 +110,14 @@
 // Compute CTAs per SM (one wave of them): with the output resident in L2,
 // two, leaving a slot for fill CTAs to run alongside; when the output streams
 // to DRAM, three (the gathers need the issue slots more than the fills).
+#ifndef BEVPOOL_FWD_WALK_DEPTH_FP8
+#define BEVPOOL_FWD_WALK_DEPTH_FP8 1      // 1: E4M3 owners load (and widen) depth values in the walk
+#endif
 #ifndef BEVPOOL_FWD_WALK_DEPTH
 #define BEVPOOL_FWD_WALK_DEPTH 1          // 1: fp16 owners load depth values in the walk (default and lean-short variants)
+#endif
+#ifndef BEVPOOL_FWD_FILL_AFTER_WAVES
+#define BEVPOOL_FWD_FILL_AFTER_WAVES 1    // output streaming to DRAM: fill CTAs follow this many waves of compute CTAs
 #endif
 #ifndef BEVPOOL_FWD_FILL_PER_SM
 #define BEVPOOL_FWD_FILL_PER_SM 4         // output streaming to DRAM: fill tiles grow until this many fill CTAs per SM
@@ -164,7 +173,8 @@ struct FwdShape {
                                      : (DT == kDtypeF16 && LEAN)         ? BEVPOOL_FWD_LEAN_BATCH
                                      : (DT == kDtypeF16 && SHORT)        ? BEVPOOL_FWD_SHORT_BATCH
                                      : (DT == kDtypeE4M3 && LEAN)        ? BEVPOOL_FWD_E4M3_LEAN_BATCH
-                                     : (DT == kDtypeF16 || VB < 16)      ? BEVPOOL_FWD_BATCH
+                                     : DT == kDtypeF16                   ? BEVPOOL_FWD_BATCH
+                                     : VB < 16                           ? BEVPOOL_FWD_E4M3_BATCH8
                                                                          : BEVPOOL_FWD_E4M3_BATCH16;
     static constexpr int BATCH = BATCH_CFG;                       // points in flight per owner
     static_assert(ROWB % VB == 0 && (VB == 2 || VB == 4 || VB == 8 || VB == 16 || VB == 32), "bad vector width");
@@ -193,6 +203,7 @@ struct FwdParams {
     FastDiv n_compute_div;        // division by n_compute
     int n_fill;                   // fill CTAs
     int fill_cells;               // cells per fill CTA
+    int fill_after;               // block index of the first fill CTA (the compute CTAs before it come first)
     unsigned char *out;           // [n_cells, C] elements of the output type
 };
 
@@ -531,16 +542,18 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
     using SM = ComputeSmem<DT, C, VAR>;
     constexpr bool LEAN = S::LEAN;
     constexpr int U = S::BATCH;                    // points in flight per owner
-    // fp16 rows in the default and lean-short variants: the owners load each
-    // point's depth value beside its row (one dependent round trip less in
-    // staging; measured: DRAM batch 93.4 -> 91.1 us L2-flushed, 86.8 -> 84.9
-    // warm; C = 128 13.7 -> 13.1 warm; BEVDet 10.0 -> 9.9 warm with six points
-    // in flight instead of eight).  The short variant keeps the staged value
-    // (canonical warm 10.5 -> 10.4 but L2-flushed 16.4 -> 16.9 us), as does the
-    // plain lean variant (8.7-point intervals: 18.1 -> 20.2 us warm), and E4M3
-    // and NVFP4 rows, which walk in a software pipeline.
-    constexpr bool WALKD = BEVPOOL_FWD_WALK_DEPTH && DT == kDtypeF16 && (VAR == kVarDefault || VAR == kVarLeanShort) &&
-                           BEVPOOL_FWD_PIPELINE == 0;
+    // fp16 rows in the default and lean-short variants, and E4M3 rows: the
+    // owners load each point's depth value beside its row (one dependent round
+    // trip less in staging; measured: DRAM batch 93.4 -> 91.1 us L2-flushed,
+    // 86.8 -> 84.9 warm; C = 128 13.7 -> 13.1 warm; BEVDet 10.0 -> 9.9 warm
+    // with six points in flight instead of eight; canonical FP8 10.5 -> 10.0
+    // warm, 572K FP8 points 19.3 -> 18.3).  The fp16 short variant keeps the
+    // staged value (canonical warm 10.5 -> 10.4 but L2-flushed 16.4 -> 16.9
+    // us), as does the plain fp16 lean variant (8.7-point intervals: 18.1 ->
+    // 20.2 us warm), and NVFP4 rows, which walk in a software pipeline.
+    constexpr bool WALKD = BEVPOOL_FWD_WALK_DEPTH &&
+                           ((DT == kDtypeF16 && (VAR == kVarDefault || VAR == kVarLeanShort) && BEVPOOL_FWD_PIPELINE == 0) ||
+                            (DT == kDtypeE4M3 && BEVPOOL_FWD_WALK_DEPTH_FP8 && BEVPOOL_FWD_PIPELINE_FP8 == 0));
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
     __shared__ int s_bounds[2];
@@ -914,9 +927,11 @@ __global__ void __launch_bounds__(kThreads, FwdShape<DT, C, VAR>::LEAN ? BEVPOOL
     grid_dep_allow();
     __shared__ __align__(16) FwdSmem<DT, C, VAR> sm;
     const int b = blockIdx.x;
-    // compute CTAs (the long ones) first, then fill CTAs in the slots they free
-    const bool compute = b < p.n_compute;
-    const int idx = compute ? b : b - p.n_compute;
+    // compute CTAs (the long ones) first, then fill CTAs in the slots they
+    // free; the fill CTAs may come after the first fill_after compute CTAs
+    const int fa = p.fill_after;
+    const bool compute = b < fa || b >= fa + p.n_fill;
+    const int idx = b < fa ? b : (compute ? b - p.n_fill : b - fa);
     if (compute)
         compute_cta<DT, C, OT, VAR>(p, idx, sm.c);
     else
@@ -1008,6 +1023,13 @@ cudaError_t launch_forward_v(const ForwardArgs &a) {
     p.n_compute_div = FastDiv(static_cast<uint32_t>(pl.n_compute));
     p.fill_cells = pl.fill_cells;
     p.n_fill = pl.n_fill;
+    p.fill_after = pl.n_compute;
+#if BEVPOOL_FWD_FILL_AFTER_WAVES
+    if (a.streaming_stores) {
+        const int64_t slots = static_cast<int64_t>(a.sm_count > 0 ? a.sm_count : 148) * pl.ctas_per_sm;
+        p.fill_after = static_cast<int>(std::min<int64_t>(pl.n_compute, slots * BEVPOOL_FWD_FILL_AFTER_WAVES));
+    }
+#endif
     p.out = static_cast<unsigned char *>(a.out);
     const int grid = p.n_compute + p.n_fill;
     const cudaError_t e = launch_dependent(k_forward<DT, C, OT, VAR>, dim3(grid), dim3(kThreads), 0, a.stream, p);
