@@ -89,15 +89,6 @@
 #ifndef BEVPOOL_FWD_LEAN_MIN_CTAS
 #define BEVPOOL_FWD_LEAN_MIN_CTAS 4       // ... with four CTAs per SM (64 registers), all computing
 #endif
-#ifndef BEVPOOL_FWD_PIPELINE
-#define BEVPOOL_FWD_PIPELINE 0            // > 0: fp16 owners walk in a two-stage pipeline of this many points
-#endif
-#ifndef BEVPOOL_FWD_PIPELINE_FP8
-#define BEVPOOL_FWD_PIPELINE_FP8 0        // the same for E4M3 rows
-#endif
-#ifndef BEVPOOL_FWD_PIPELINE_NVFP4
-#define BEVPOOL_FWD_PIPELINE_NVFP4 2      // the same for NVFP4 rows
-#endif
 #ifndef BEVPOOL_FWD_MULTIWAVE
 #define BEVPOOL_FWD_MULTIWAVE 64          // > 0: compute CTAs of at most a round less this many points each
 #endif
@@ -550,10 +541,10 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
     // warm, 572K FP8 points 19.3 -> 18.3).  The fp16 short variant keeps the
     // staged value (canonical warm 10.5 -> 10.4 but L2-flushed 16.4 -> 16.9
     // us), as does the plain fp16 lean variant (8.7-point intervals: 18.1 ->
-    // 20.2 us warm), and NVFP4 rows, which walk in a software pipeline.
+    // 20.2 us warm), and NVFP4 rows (canonical 11.8 -> 12.3 us warm).
     constexpr bool WALKD = BEVPOOL_FWD_WALK_DEPTH &&
-                           ((DT == kDtypeF16 && (VAR == kVarDefault || VAR == kVarLeanShort) && BEVPOOL_FWD_PIPELINE == 0) ||
-                            (DT == kDtypeE4M3 && BEVPOOL_FWD_WALK_DEPTH_FP8 && BEVPOOL_FWD_PIPELINE_FP8 == 0));
+                           ((DT == kDtypeF16 && (VAR == kVarDefault || VAR == kVarLeanShort)) ||
+                            (DT == kDtypeE4M3 && BEVPOOL_FWD_WALK_DEPTH_FP8));
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
     __shared__ int s_bounds[2];
@@ -752,87 +743,11 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
                         }
                     }
                 };
-                // software pipeline (not in the 64-register lean variant): the
-                // next group's rows are in flight while this group's FMAs run
-                // (two register buffers of PU points)
-                constexpr int PU = LEAN                   ? 0
-                                   : DT == kDtypeE4M3     ? BEVPOOL_FWD_PIPELINE_FP8
-                                   : DT == kDtypeNVFP4    ? BEVPOOL_FWD_PIPELINE_NVFP4
-                                                          : BEVPOOL_FWD_PIPELINE;
-                if constexpr (PU > 0) {
-                struct Grp {
-                    uint32_t df[PU];
-                    RawVec<S::VB> f[PU];
-                    [[maybe_unused]] unsigned short sh[PU];
-                };
-                auto fetch = [&](Grp &g, int v) {
-                    int rows[PU];
-#pragma unroll
-                    for (int kk = 0; kk < PU; ++kk) {
-                        if (v + kk < end) {
-                            const int2 q = *reinterpret_cast<const int2 *>(&sm.rec[v + kk]);
-                            rows[kk] = q.x;
-                            g.df[kk] = static_cast<uint32_t>(q.y);
-                        } else {
-                            rows[kk] = 0;
-                            g.df[kk] = kSkipBit;
-                        }
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < PU; ++kk) {
-                        if (v + kk < end) {
-                            g.f[kk] = load_vec<S::VB>(featp + static_cast<int64_t>(rows[kk]) * S::ROWB);
-                            if constexpr (S::NV) {
-                                const unsigned char sc = __ldg(blockp + static_cast<int64_t>(rows[kk]) * (C / 16));
-                                g.sh[kk] = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sc), __NV_E4M3).x;
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < RawVec<S::VB>::NW; ++i) g.f[kk].w[i] = 0u;
-                            if constexpr (S::NV) g.sh[kk] = 0;
-                        }
-                    }
-                };
-                auto consume = [&](const Grp &g, int v) {
-#pragma unroll
-                    for (int kk = 0; kk < PU; ++kk) {
-                        unsigned short d = static_cast<unsigned short>(g.df[kk] & 0xffffu);
-                        if constexpr (S::NV) d = mul_f16_bits(d, g.sh[kk]);
-                        if (!(g.df[kk] & kSkipBit)) fma_vec<DT, S::VB>(acc, d, g.f[kk]);
-                        if (g.df[kk] & kEndBit) {
-                            if (to_slot) {
-                                float *dst = &sm.slot[o][ol * S::EPL];
-#pragma unroll
-                                for (int e = 0; e < S::EPL; ++e) dst[e] = acc[e];
-                                to_slot = false;
-                            } else {
-                                store_interval<OT, C, S::EPL>(p, sm.rec[v + kk].bev, ol, acc, mode,
-                                                              !(g.df[kk] & kNoCellBit));
-                            }
-#pragma unroll
-                            for (int e = 0; e < S::EPL; ++e) acc[e] = 0.f;
-                        }
-                    }
-                };
-                Grp ga, gb;
-                fetch(ga, beg);
-                for (int v = beg;;) {
-                    if (v + PU < end) fetch(gb, v + PU);
-                    consume(ga, v);
-                    v += PU;
-                    if (v >= end) break;
-                    if (v + PU < end) fetch(ga, v + PU);
-                    consume(gb, v);
-                    v += PU;
-                    if (v >= end) break;
+                int v = beg;
+                if (!checked) {
+                    for (; v + U <= end; v += U) walk(v, U, std::true_type{});
                 }
-                } else {
-                    int v = beg;
-                    if (!checked) {
-                        for (; v + U <= end; v += U) walk(v, U, std::true_type{});
-                    }
-                    for (; v < end; v += U) walk(v, min(U, end - v), std::false_type{});
-                }
+                for (; v < end; v += U) walk(v, min(U, end - v), std::false_type{});
                 const bool cut = (sm.rec[end - 1].dflags & kEndBit) == 0u;   // the share ends inside an interval
                 st = head ? kHead : (to_slot && cut ? kPass : kCont);
                 if (cut) {
