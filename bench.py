@@ -638,6 +638,18 @@ def run_ours(args) -> None:
         achieved_l2 = bm0["gather"] / (warm_us * 1e-6) / 1e9
         rd, wr = bm0["gather"] - bm0["out"], bm0["out"]
         ceiling = (rd + wr) / (rd / NCU_L2_READ_GBS + wr / NCU_L2_WRITE_GBS)
+        gather_probe = None
+        row_bytes = wl.C // 2 if wl.dtype == "nvfp4" else wl.C * (2 if wl.dtype == "f16" else 1)
+        if row_bytes % 16 == 0 and row_bytes <= 512 and n_pts > 0:
+            # the forward's row gather alone over this map's ranks_feat (what its walk can reach)
+            rows = m.ranks_feat[:n_pts]
+            g_us = graph_us(lambda: bevpool.probe_gather(feat, row_bytes, rows, ctas_per_sm=3), stream, calls=20,
+                            reps=5)
+            gather_probe = {"time_us": g_us, "bytes": n_pts * row_bytes,
+                            "gbs": n_pts * row_bytes / (g_us * 1e-6) / 1e9,
+                            "what": "bevpool_probe_gather: the forward's feature-row gather alone (16-byte lanes, "
+                                    "8 rows in flight, 3 CTAs per SM) over this map's ranks_feat, warm L2, "
+                                    "CUDA-graph median per launch"}
         roof_l2 = {"bound": "l2", "achieved": achieved_l2, "peak": probe["copy_gbs"], "unit": "GB/s",
                    "frac": achieved_l2 / probe["copy_gbs"], "traffic": None, "kernel": "k_forward",
                    "bytes_per_launch": bm0["gather"], "time_us": warm_us,
@@ -647,7 +659,7 @@ def run_ours(args) -> None:
                    "ncu_ceiling_gbs": ceiling, "frac_of_ncu_ceiling": achieved_l2 / ceiling,
                    "ncu_ceiling_source": "188 L2 slices x (2 read | 1 write) sectors of 32 B per cycle x "
                                          "1.979 GHz, weighted by this forward's read and write bytes",
-                   "probe": probe}
+                   "probe": probe, "gather_probe": gather_probe}
 
     dram_batch = None
     if wl.name == "canonical" and not args.no_dram_batch and not e4m3_out:

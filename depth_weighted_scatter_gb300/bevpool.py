@@ -75,6 +75,8 @@ _lib.bevpool_validate_map.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
 _lib.bevpool_validate_map.restype = ctypes.c_int
 _lib.bevpool_probe_l2.argtypes = [_i32, _vp, _sz, _i32, _vp, _vp]
 _lib.bevpool_probe_l2.restype = ctypes.c_int
+_lib.bevpool_probe_gather.argtypes = [_vp, _i32, _i32, _vp, _i32, _i32, _vp, _vp]
+_lib.bevpool_probe_gather.restype = ctypes.c_int
 
 
 class BevpoolError(RuntimeError):
@@ -373,3 +375,21 @@ def probe_l2(buf, passes: int, *, mode: int = PROBE_READ, sink=None, stream=None
                           _stream(stream))
     if st != BEVPOOL_OK:
         raise BevpoolError(st, "bevpool_probe_l2")
+
+
+def bevpool_probe_gather(feat: int, n_rows: int, row_bytes: int, rows: int, n_points: int, ctas_per_sm: int,
+                         d_sink: int, stream: int) -> int:
+    return _lib.bevpool_probe_gather(feat, n_rows, row_bytes, rows, n_points, ctas_per_sm, d_sink, stream)
+
+
+def probe_gather(feat, row_bytes: int, rows, *, ctas_per_sm: int = 3, sink=None, stream=None):
+    """One launch of the gather probe over the rows of `feat` (a device
+    tensor of n_rows * row_bytes bytes) listed in `rows` (device int32);
+    adds the sum of the gathered words to `sink` (device int32, zeroed by the
+    caller), or with no sink runs the timing mode."""
+    n_rows = feat.numel() * feat.element_size() // row_bytes
+    st = bevpool_probe_gather(feat.data_ptr(), n_rows, row_bytes, rows.data_ptr(), rows.numel(), ctas_per_sm,
+                              sink.data_ptr() if sink is not None else 0, _stream(stream))
+    if st != BEVPOOL_OK:
+        raise BevpoolError(st, "bevpool_probe_gather")
+    return sink

@@ -15,6 +15,15 @@
 // Copy: the second half of the buffer receives the first half, word by word
 // XORed with p * 0x9E3779B9 in pass p (so every pass writes new values), with
 // the loads of the read probe and the stores of the write probe.
+//
+// Gather (bevpool_probe_gather): the feature-row gather of the forward alone,
+// in the forward's lane layout (owners of row_bytes / 16 lanes, one 16-byte
+// vector a lane, eight rows in flight, each owner a contiguous equal share of
+// the points), over a caller's row list (a map's ranks_feat), with nothing
+// else: no depth, no accumulation into rows, no stores.  The words it read
+// are summed (mod 2^32) into *d_sink, or, with no sink (the timing mode),
+// only kept live so no load is dropped.  It bounds what the forward's walk
+// can reach on the same rows.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -104,10 +113,82 @@ __global__ void __launch_bounds__(kThreads) k_probe_copy(const uint4 *src, uint4
     }
 }
 
+constexpr int kGatherBatch = 8;               // rows in flight per owner
+
+__global__ void __launch_bounds__(kThreads) k_probe_gather(const unsigned char *feat, int32_t n_rows, int row_bytes,
+                                                           const int32_t *rows, int32_t n_points, uint32_t *sink) {
+    const int lpo = row_bytes / 16;               // lanes per owner (1..32)
+    const int opw = 32 / lpo;                     // owners per warp
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int og = lane / lpo, ol = lane - og * lpo;
+    uint32_t s = 0;
+    if (og < opw) {
+        const int64_t owners = static_cast<int64_t>(gridDim.x) * kWarps * opw;
+        const int64_t o = (static_cast<int64_t>(blockIdx.x) * kWarps + warp) * opw + og;
+        const int64_t share = (n_points + owners - 1) / owners;
+        const int64_t beg = min(static_cast<int64_t>(n_points), o * share);
+        const int64_t end = min(static_cast<int64_t>(n_points), beg + share);
+        const unsigned char *base = feat + ol * 16;
+        int64_t t = beg;
+        for (; t + kGatherBatch <= end; t += kGatherBatch) {
+            int r[kGatherBatch];
+#pragma unroll
+            for (int k = 0; k < kGatherBatch; ++k) r[k] = __ldg(rows + t + k);
+            uint4 v[kGatherBatch];
+#pragma unroll
+            for (int k = 0; k < kGatherBatch; ++k) {
+                const bool ok = r[k] >= 0 && r[k] < n_rows;
+                v[k] = ok ? __ldg(reinterpret_cast<const uint4 *>(base + static_cast<int64_t>(r[k]) * row_bytes))
+                          : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int k = 0; k < kGatherBatch; ++k) s += word_sum(v[k]);
+        }
+        for (; t < end; ++t) {
+            const int r = __ldg(rows + t);
+            if (r >= 0 && r < n_rows)
+                s += word_sum(__ldg(reinterpret_cast<const uint4 *>(base + static_cast<int64_t>(r) * row_bytes)));
+        }
+    }
+    if (!sink) {                                  // timing: keep the sum live, no atomics, no barrier
+        asm volatile("" ::"r"(s));
+        return;
+    }
+    // one atomic per CTA (thousands of warps adding to one word would queue
+    // at its L2 slice)
+    __shared__ uint32_t part[kWarps];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) part[warp] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t t = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) t += part[w];
+        atomicAdd(sink, t);
+    }
+}
+
 }  // namespace
 }  // namespace bevpool
 
 using namespace bevpool;
+
+extern "C" BEVPOOL_API bevpool_status bevpool_probe_gather(const void *feat, int32_t n_rows, int32_t row_bytes,
+                                                           const int32_t *rows, int32_t n_points,
+                                                           int32_t ctas_per_sm, uint32_t *d_sink, void *stream) {
+    if (!feat || reinterpret_cast<uintptr_t>(feat) % 16 != 0 || n_rows < 1 || row_bytes < 16 || row_bytes > 512 ||
+        row_bytes % 16 != 0 || n_points < 0 || (n_points > 0 && !rows) ||
+        reinterpret_cast<uintptr_t>(rows) % 4 != 0 || ctas_per_sm < 1 || ctas_per_sm > 8)
+        return BEVPOOL_ERR_INVALID_ARG;
+    DeviceInfo info;
+    if (!device_info(&info)) return BEVPOOL_ERR_CUDA;
+    const unsigned grid = static_cast<unsigned>(info.sm_count * ctas_per_sm);
+    k_probe_gather<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const unsigned char *>(feat), n_rows, row_bytes, rows, n_points, d_sink);
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? BEVPOOL_OK : BEVPOOL_ERR_CUDA;
+}
 
 extern "C" BEVPOOL_API bevpool_status bevpool_probe_l2(int32_t mode, void *buf, size_t bytes, int32_t passes,
                                                        uint32_t *d_sink, void *stream) {

@@ -378,6 +378,29 @@ BEVPOOL_API bevpool_status bevpool_validate_map(const int32_t *ranks_depth, cons
 BEVPOOL_API bevpool_status bevpool_probe_l2(int32_t mode, void *buf, size_t bytes, int32_t passes,
                                 uint32_t *d_sink, void *stream);
 
+/*
+ * Gather probe (a measurement helper, not part of the pooling path): the
+ * forward's feature-row gather alone, over a caller's row list (normally a
+ * map's ranks_feat), in the forward's lane layout: owners of row_bytes / 16
+ * lanes, one 16-byte vector a lane, eight rows in flight per owner, each
+ * owner a contiguous equal share of the points; no depth, no accumulation
+ * into output rows, no stores.  It bounds the rate the forward's walk can
+ * reach on the same rows (the gather of "Optimize for large L2 caches").
+ *   feat         device, 16-byte aligned, n_rows rows of row_bytes bytes;
+ *   row_bytes    a multiple of 16 in [16, 512];
+ *   rows         device int32[n_points]; rows outside [0, n_rows) are skipped;
+ *   ctas_per_sm  256-thread CTAs per SM in the launch, 1..8;
+ *   d_sink       device uint32 the caller zeroes first; the launch adds the
+ *                sum (mod 2^32) of the 32-bit words of every gathered row.
+ *                NULL: the timing mode (the sum is formed but not written, so
+ *                no atomic or barrier enters the measured time).
+ * One launch on `stream`.  Returns BEVPOOL_ERR_INVALID_ARG for a bad
+ * argument (nothing launched), BEVPOOL_ERR_CUDA if the launch fails.
+ */
+BEVPOOL_API bevpool_status bevpool_probe_gather(const void *feat, int32_t n_rows, int32_t row_bytes,
+                                                const int32_t *rows, int32_t n_points, int32_t ctas_per_sm,
+                                                uint32_t *d_sink, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -71,3 +71,43 @@ def test_probe_counts_one_launch(bp):
     bp.probe_l2(buf, 1, sink=sink)
     torch.cuda.synchronize()
     assert bp.bevpool_kernel_launches() == before + 1
+
+
+@pytest.mark.parametrize("row_bytes,n_rows,n_points,ctas", [(16, 5, 1, 1), (160, 16_896, 7, 3), (160, 16_896, 100_003, 3),
+                                                            (256, 1_000, 20_000, 8), (512, 333, 4_097, 2),
+                                                            (96, 50, 0, 3)])
+def test_gather_probe_reads_every_listed_row(bp, row_bytes, n_rows, n_points, ctas):
+    """The gather probe adds the word sum of every listed row (once per listing,
+    rows out of range skipped) to the sink."""
+    import torch
+
+    rng = np.random.default_rng(row_bytes * 7 + n_points)
+    words = rng.integers(0, 2**32, size=n_rows * row_bytes // 4, dtype=np.uint64).astype(np.uint32)
+    rows = rng.integers(-2, n_rows + 2, size=max(n_points, 1)).astype(np.int32)[:n_points]
+    feat = torch.from_numpy(words.view(np.int32)).cuda()
+    rows_d = torch.from_numpy(rows).cuda() if n_points else torch.zeros(1, dtype=torch.int32, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = bp.bevpool_probe_gather(feat.data_ptr(), n_rows, row_bytes, rows_d.data_ptr(), n_points, ctas,
+                                 sink.data_ptr(), 0)
+    assert st == bp.BEVPOOL_OK
+    got = int(sink.cpu().numpy().view(np.uint32)[0])
+    row_sums = words.reshape(n_rows, row_bytes // 4).astype(np.uint64).sum(axis=1)
+    valid = rows[(rows >= 0) & (rows < n_rows)]
+    assert got == int(row_sums[valid].sum()) % 2**32
+
+
+def test_gather_probe_rejects_bad_arguments(bp):
+    import torch
+
+    feat = torch.zeros(1024, dtype=torch.int32, device="cuda")
+    rows = torch.zeros(4, dtype=torch.int32, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ok = lambda **kw: bp.bevpool_probe_gather(*[kw.get(k, v) for k, v in dict(
+        feat=feat.data_ptr(), n_rows=16, row_bytes=256, rows=rows.data_ptr(), n=4, ctas=3, sink=sink.data_ptr(),
+        stream=0).items()])
+    assert ok() == bp.BEVPOOL_OK
+    assert ok(row_bytes=24) == bp.BEVPOOL_ERR_INVALID_ARG
+    assert ok(row_bytes=528) == bp.BEVPOOL_ERR_INVALID_ARG
+    assert ok(ctas=9) == bp.BEVPOOL_ERR_INVALID_ARG
+    assert ok(sink=0) == bp.BEVPOOL_OK                    # the timing mode
+    assert ok(feat=feat.data_ptr() + 4) == bp.BEVPOOL_ERR_INVALID_ARG
