@@ -456,7 +456,16 @@ def graph_us(call, stream, calls: int = 100, reps: int = 10) -> float:
     return statistics.median(out)
 
 
-def dram_batch_forward(device, stream, flush, steps: int) -> dict:
+def l2_gather_roofline(bm: dict, time_us: float, probe: dict, time_note: str) -> dict:
+    """The L2 roofline of the gather-level bytes (what the owners read and
+    write at the L2) over a forward time, against the probe's copy bandwidth."""
+    achieved = bm["gather"] / (time_us * 1e-6) / 1e9
+    return {"bound": "l2", "achieved": achieved, "peak": probe["copy_gbs"], "unit": "GB/s",
+            "frac": achieved / probe["copy_gbs"], "bytes_per_launch": bm["gather"], "time_us": time_us,
+            "time": time_note, "peak_source": "bevpool_probe_l2 copy (read + write bytes), 64 MiB resident, this run"}
+
+
+def dram_batch_forward(device, stream, flush, steps: int, probe=None) -> dict:
     """The DRAM-bound batch configuration (4 x canonical frustum, C = 128,
     [4, 512, 512, 128] output, ~334 MB of compulsory traffic, above the L2):
     its forward timed with L2 flushed before each call, and its HBM roofline."""
@@ -484,6 +493,8 @@ def dram_batch_forward(device, stream, flush, steps: int) -> dict:
     us = statistics.mean(ms) * 1e3
     peak, peak_kind = measured_peaks()
     achieved = bm["footprint"] / (us * 1e-6) / 1e9
+    roof_l2 = (l2_gather_roofline(bm, us, probe, "mean event time per call, L2 flushed before each")
+               if probe is not None else None)
     return {"workload": f"{wl.name}: NC={wl.NC} D={wl.D} H={wl.H} W={wl.W} C={wl.C} grid={wl.grid} "
                         f"points={m.n_points} intervals={m.n_intervals}",
             "forward_us": us, "forward_us_median": statistics.median(ms) * 1e3, "calls": steps,
@@ -493,6 +504,7 @@ def dram_batch_forward(device, stream, flush, steps: int) -> dict:
                          "frac": achieved / peak, "traffic": recorded_traffic("dram_batch"), "kernel": "k_forward",
                          "bytes_per_launch": bm["footprint"],
                          "peak_source": f"hbm_gbs of MEASURED_PEAKS.json ({peak_kind})"},
+            "roofline_l2_gather": roof_l2,
             "clocks": clocks}
 
 
@@ -633,8 +645,8 @@ def run_ours(args) -> None:
     roof_l2 = None
     l2_bytes = torch.cuda.get_device_properties(device).L2_cache_size
     bm0 = bytes_model(wl, n_pts, n_int, 1 if e4m3_out else 2)
+    probe = l2_probe(device, stream)
     if bm0["footprint"] <= l2_bytes // 2 and isinstance(warm_us, float):
-        probe = l2_probe(device, stream)
         achieved_l2 = bm0["gather"] / (warm_us * 1e-6) / 1e9
         rd, wr = bm0["gather"] - bm0["out"], bm0["out"]
         ceiling = (rd + wr) / (rd / NCU_L2_READ_GBS + wr / NCU_L2_WRITE_GBS)
@@ -663,7 +675,7 @@ def run_ours(args) -> None:
 
     dram_batch = None
     if wl.name == "canonical" and not args.no_dram_batch and not e4m3_out:
-        dram_batch = dram_batch_forward(device, stream, flush, steps=max(3, min(args.steps, 50)))
+        dram_batch = dram_batch_forward(device, stream, flush, steps=max(3, min(args.steps, 50)), probe=probe)
 
     # End to end through the C ABI from pinned host buffers: every frame copies
     # its depth and features in, runs the forward and reads its output back.
@@ -727,6 +739,9 @@ def run_ours(args) -> None:
         "config": config_dict(wl, n_pts, n_int, world, args.out_dtype),
         "roofline": roof_l2 if roof_l2 is not None else roof_hbm,
         "roofline_hbm": roof_hbm,
+        "roofline_l2_gather": (l2_gather_roofline(bm, fwd_mean * 1e3, probe, "mean event time per call, L2 flushed "
+                                                  "before each (the working set exceeds half the L2)")
+                               if roof_l2 is None else None),
         "dram_batch": dram_batch,
         "cpu_baseline": (cpu_oracle_time(wl, out_scale=out_scale)
                          if (world == 1 and not args.no_cpu_baseline) else None),
