@@ -57,7 +57,8 @@ def test_plans_of_the_five_configurations():
     assert (bevdet["variant"], bevdet["n_compute"], bevdet["fill_cells"], bevdet["n_fill"]) == (DEFAULT, 304, 128, 128)
     dram = plan(bp.BEVPOOL_F16, 128, 2_198_618, 738_763, 1 << 20, dims=dict(NC=24, D=118, H=32, W=88))
     assert (dram["variant"], dram["ctas_per_sm"], dram["n_compute"], dram["fill_cells"], dram["n_fill"],
-            dram["streaming"]) == (LEAN_SHORT, 4, 2432, 1024, 1024, 1)
+            dram["streaming"]) == (LEAN_SHORT, 4, 1824, 1024, 1024, 1)
+    assert dram["round"] == 1280 and canon["round"] == 1024 and bevdet["round"] == 1280 and fp8["round"] == 1024
     tiny = plan(bp.BEVPOOL_F16, 8, 190, 150, 256, dims=dict(NC=1, D=8, H=4, W=8))
     assert tiny["n_compute"] == 1 and tiny["n_fill"] == 2 and tiny["streaming"] == 0
 
@@ -155,13 +156,17 @@ def test_compute_cta_count(dtype, C):
             assert -(-n // p["n_compute"]) <= p["round"] - 64
         else:
             assert p["n_compute"] == max(1, one_wave)
-        assert p["round"] % 256 == 0 and 256 <= p["round"] <= 1024
+        assert p["round"] % 256 == 0 and 256 <= p["round"] <= (1280 if dtype == bp.BEVPOOL_F16 else 1024)
 
 
 def test_rounds_fit_the_shared_memory_of_wide_rows():
-    """Rows of 256 channels leave room for full rounds of 1024 points."""
+    """Rows of 256 channels leave room for full rounds: 1280 points for the fp16
+    default and lean-short variants, 1024 for the other variants and dtypes."""
     for dtype in (bp.BEVPOOL_F16, bp.BEVPOOL_E4M3, bp.BEVPOOL_NVFP4):
-        assert plan(dtype, 256, 210_000, 57_000, 129_600)["round"] == 1024
+        p = plan(dtype, 256, 210_000, 57_000, 129_600)
+        wide = dtype == bp.BEVPOOL_F16 and p["variant"] in (DEFAULT, LEAN_SHORT)
+        assert p["round"] == (1280 if wide else 1024)
+    assert plan(bp.BEVPOOL_F16, 256, 210_000, 20_000, 129_600)["round"] == 1024      # the plain lean variant
 
 
 # ------------------------------------------------------------------ fill tiles
