@@ -107,6 +107,9 @@
 #ifndef BEVPOOL_FWD_WALK_DEPTH
 #define BEVPOOL_FWD_WALK_DEPTH 1          // 1: fp16 owners load depth values in the walk (default and lean-short variants)
 #endif
+#ifndef BEVPOOL_FWD_COMBINE_BATCH
+#define BEVPOOL_FWD_COMBINE_BATCH 2       // owners whose partial rows the combine loads at a time
+#endif
 #ifndef BEVPOOL_FWD_ROUND_MAX_WIDE
 #define BEVPOOL_FWD_ROUND_MAX_WIDE 1280   // points per staged round at most, fp16 default and lean-short variants
 #endif
@@ -542,7 +545,6 @@ template <int DT, int C, int OT, int VAR>
 __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, ComputeSmem<DT, C, VAR> &sm) {
     using S = FwdShape<DT, C, VAR>;
     using SM = ComputeSmem<DT, C, VAR>;
-    constexpr bool LEAN = S::LEAN;
     constexpr int U = S::BATCH;                    // points in flight per owner
     // fp16 rows in the default and lean-short variants, and E4M3 rows: the
     // owners load each point's depth value beside its row (one dependent round
@@ -782,17 +784,35 @@ __device__ __forceinline__ void compute_cta(const FwdParams &p, int cidx, Comput
         // adds the slots of owners o2, o2 + 1, ... to a until one of them ends
         // the interval (then stores it) or the round ends (then carries it)
         auto finish = [&](float *a, int o2, int bev) {
-            for (; o2 < S::OWNERS; ++o2) {
-                const int st2 = sm.state[o2];
-                if (st2 == kHead || st2 == kEmpty) break;
-                const float *q = &sm.slot[o2][ol * S::EPL];
+            // the states and slots of CB owners are loaded together, then
+            // added in owner order (the same order and sums as one at a time):
+            // an interval that spans many owners (BEVDet: up to 464 points)
+            // waits on half as many dependent shared loads (measured warm:
+            // BEVDet 8.2 -> 7.9 us; the plain lean variant keeps one at a
+            // time, 572K points 17.9 -> 18.1 us with two)
+            constexpr int CB = VAR == kVarLean ? 1 : BEVPOOL_FWD_COMBINE_BATCH;
+            for (; o2 < S::OWNERS; o2 += CB) {
+                int st[CB];
+                float q[CB][S::EPL];
 #pragma unroll
-                for (int e = 0; e < S::EPL; ++e) a[e] += q[e];
-                if (st2 == kCont) {
-                    store_interval<OT, C, S::EPL>(p, bev, ol, a, mode, bev >= 0 && bev < p.n_cells);
-                    return;
+                for (int j = 0; j < CB; ++j) {
+                    const int oj = o2 + j < S::OWNERS ? o2 + j : S::OWNERS - 1;   // in bounds; unused past the end
+                    st[j] = o2 + j < S::OWNERS ? sm.state[oj] : kHead;
+#pragma unroll
+                    for (int e = 0; e < S::EPL; ++e) q[j][e] = sm.slot[oj][ol * S::EPL + e];
+                }
+#pragma unroll
+                for (int j = 0; j < CB; ++j) {
+                    if (st[j] == kHead || st[j] == kEmpty) goto carry_out;
+#pragma unroll
+                    for (int e = 0; e < S::EPL; ++e) a[e] += q[j][e];
+                    if (st[j] == kCont) {
+                        store_interval<OT, C, S::EPL>(p, bev, ol, a, mode, bev >= 0 && bev < p.n_cells);
+                        return;
+                    }
                 }
             }
+        carry_out:
             float *dst = &sm.carry[cb ^ 1][ol * S::EPL];
 #pragma unroll
             for (int e = 0; e < S::EPL; ++e) dst[e] = a[e];
