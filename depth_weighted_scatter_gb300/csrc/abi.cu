@@ -145,7 +145,7 @@ const char *bevpool_status_string(bevpool_status status) {
     }
 }
 
-int32_t bevpool_version(void) { return 200; }   // 0.2.0: E4M3 output, NVFP4 features, per-frame call
+int32_t bevpool_version(void) { return 300; }   // 0.3.0: launch-plan query, gather probe
 
 int64_t bevpool_kernel_launches(void) { return g_kernel_launches.load(std::memory_order_relaxed); }
 
