@@ -50,7 +50,11 @@ inline bool frustum_points(int32_t NC, int32_t D, int32_t H, int32_t W, int64_t 
 // (once every CTA of that kernel has called grid_dep_allow() or exited); its
 // grid_dep_wait() then blocks until the previous kernel has completed and its
 // writes are visible.  In a kernel launched normally grid_dep_wait() returns
-// at once.  Every kernel here waits before touching any data.
+// at once.  Every kernel here waits before touching data an earlier kernel
+// of the call writes; the map build's counting and scatter passes read their
+// block of the caller's cell ids first (written before the call began, so
+// complete and visible once the first kernel of the call has passed its own
+// wait, which comes before that kernel lets its dependants start).
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_allow() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

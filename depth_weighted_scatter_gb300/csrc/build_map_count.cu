@@ -116,12 +116,12 @@ __device__ __forceinline__ void load_block(const int32_t *__restrict__ cell_ids,
 __global__ void __launch_bounds__(kThreads)
 k_count_cells(const int32_t *__restrict__ cell_ids, int64_t nf, int32_t n_cells, bool vec,
               int32_t *__restrict__ count, int32_t *__restrict__ invalid) {
-    grid_dep_wait();
-    grid_dep_allow();
     __shared__ long long red[kWarps];
     const int64_t first = static_cast<int64_t>(blockIdx.x) * kTile + static_cast<int64_t>(threadIdx.x) * kItems;
     int c[kItems];
-    load_block(cell_ids, nf, vec, first, c);
+    load_block(cell_ids, nf, vec, first, c);       // the caller's input: read while k_zero drains
+    grid_dep_wait();
+    grid_dep_allow();
     int bad = 0;
 #pragma unroll
     for (int j = 0; j < kItems; ++j) {
@@ -212,11 +212,11 @@ k_offsets(const int32_t *__restrict__ count, int32_t n_cells, const int32_t *__r
 __global__ void __launch_bounds__(kThreads)
 k_scatter(const int32_t *__restrict__ cell_ids, int64_t nf, int32_t n_cells, bool vec,
           int32_t *__restrict__ cursor, int32_t *__restrict__ tmp_p) {
-    grid_dep_wait();
-    grid_dep_allow();
     const int64_t first = static_cast<int64_t>(blockIdx.x) * kTile + static_cast<int64_t>(threadIdx.x) * kItems;
     int c[kItems];
-    load_block(cell_ids, nf, vec, first, c);
+    load_block(cell_ids, nf, vec, first, c);       // the caller's input: read while k_offsets drains
+    grid_dep_wait();
+    grid_dep_allow();
     int pos[kItems];
 #pragma unroll
     for (int j = 0; j < kItems; ++j) pos[j] = (c[j] >= 0 && c[j] < n_cells) ? atomicAdd(cursor + c[j], 1) : -1;
