@@ -21,7 +21,7 @@
 //                    points in registers (a bitonic network); longer
 //                    intervals go to two work lists;
 //   7. k_sort_lists  persistent CTAs drain the lists: a warp ranks an interval
-//                    of up to 64 points by counting (rank = number of smaller
+//                    of up to 128 points by counting (rank = number of smaller
 //                    values), a CTA sorts up to 8192 in shared memory
 //                    (bitonic), and beyond that the CTA rebuilds the run by
 //                    scanning the frustum in order for that cell.
@@ -41,7 +41,20 @@ constexpr int kTile = kThreads * kItems;        // 4096 frustum points per CTA t
 constexpr int kCellItems = 4;
 constexpr int kCellTile = kThreads * kCellItems; // 1024 cells per scan tile
 constexpr int kThreadSortMax = 16;              // longest interval one thread sorts in registers
-constexpr int kWarpSortMax = 64;                // longest interval a warp ranks
+// Intervals of 65..128 points are ranked by one warp (four values a lane)
+// rather than sorted by a CTA in shared memory, and the list pass runs six
+// CTAs per SM (its residency) instead of four.  Measured, L2 flushed: Table-1
+// very large (2,377 such intervals) 101.6 -> 85.9 us, Table-1 large 49.1 ->
+// 47.4, canonical and BEVDet unchanged; a warp for up to 256 points was
+// slower (BEVDet 43.1 -> 52.2 us: eight values a lane).
+#ifndef BEVPOOL_MAP_WARP_SORT_MAX
+#define BEVPOOL_MAP_WARP_SORT_MAX 128
+#endif
+#ifndef BEVPOOL_MAP_LIST_CTAS_PER_SM
+#define BEVPOOL_MAP_LIST_CTAS_PER_SM 6
+#endif
+constexpr int kWarpSortMax = BEVPOOL_MAP_WARP_SORT_MAX;   // longest interval a warp ranks (a multiple of 32, <= 128)
+static_assert(kWarpSortMax % 32 == 0 && kWarpSortMax >= 64 && kWarpSortMax <= 128, "warp sorts hold 2..4 values a lane");
 constexpr int kCtaSortMax = 8192;               // longest interval sorted in shared memory
 
 struct CountWs {
@@ -53,8 +66,8 @@ struct CountWs {
     int32_t *tile_nz;     // [cell tiles]
     int32_t *invalid;     // [1]
     int32_t *lists;       // [2]: entries in mid_list, long_list
-    int32_t *mid_list;    // [min(n_frustum, n_cells)] intervals of 17..64 points
-    int32_t *long_list;   // [min(n_frustum, n_cells)] intervals of more than 64 points
+    int32_t *mid_list;    // [min(n_frustum, n_cells)] intervals of 17..kWarpSortMax points
+    int32_t *long_list;   // [min(n_frustum, n_cells)] intervals of more than kWarpSortMax points
 };
 
 size_t carve(void *base, int64_t nf, int32_t n_cells, CountWs *ws) {
@@ -267,7 +280,7 @@ __device__ __forceinline__ void warp_rank_sort(const int32_t *__restrict__ src, 
     }
 }
 
-// The CTA sorts an interval of 64 < L <= 8192 points in shared memory.
+// The CTA sorts an interval of kWarpSortMax < L <= 8192 points in shared memory.
 __device__ __forceinline__ void cta_bitonic_sort(const int32_t *__restrict__ src, int s, int L, int cell,
                                                  const Derive &out, int *buf) {
     int n2 = 1;
@@ -385,10 +398,13 @@ k_sort_lists(const int32_t *__restrict__ tmp_p, const int32_t *__restrict__ star
     for (int x = blockIdx.x * kWarps + (threadIdx.x >> 5); x < n_mid; x += warps_total) {   // warp-uniform
         const int j = __ldg(mid_list + x);
         const int L = __ldg(lengths + j);
+        const int s = __ldg(starts + j), cell = __ldg(icell + j);
         if (L <= 32)
-            warp_rank_sort<1>(tmp_p, __ldg(starts + j), L, __ldg(icell + j), out);
+            warp_rank_sort<1>(tmp_p, s, L, cell, out);
+        else if (L <= 64)
+            warp_rank_sort<2>(tmp_p, s, L, cell, out);
         else
-            warp_rank_sort<2>(tmp_p, __ldg(starts + j), L, __ldg(icell + j), out);
+            warp_rank_sort<4>(tmp_p, s, L, cell, out);
     }
     for (int x = blockIdx.x; x < n_long; x += gridDim.x) {                                // CTA-uniform
         const int j = __ldg(long_list + x);
@@ -447,7 +463,7 @@ cudaError_t launch_build_map_counting(const BuildMapArgs &a) {
                              ws.mid_list, ws.long_list, out);
     count_launch();
     if (e == cudaSuccess)
-        e = launch_dependent(k_sort_lists, dim3(info.sm_count * 4), dim3(kThreads), 0, st, ws.tmp_p,
+        e = launch_dependent(k_sort_lists, dim3(info.sm_count * BEVPOOL_MAP_LIST_CTAS_PER_SM), dim3(kThreads), 0, st, ws.tmp_p,
                              a.interval_starts, a.interval_lengths, ws.icell, ws.lists, ws.mid_list, ws.long_list,
                              a.cell_ids, nf, out);
     count_launch();
