@@ -20,11 +20,12 @@
 //                    ranks_bev: one thread sorts an interval of up to 16
 //                    points in registers (a bitonic network); longer
 //                    intervals go to two work lists;
-//   7. k_sort_lists  persistent CTAs drain the lists: a warp ranks an interval
-//                    of up to 128 points by counting (rank = number of smaller
-//                    values), a CTA sorts up to 8192 in shared memory
-//                    (bitonic), and beyond that the CTA rebuilds the run by
-//                    scanning the frustum in order for that cell.
+//   7. k_sort_lists  persistent CTAs drain the lists: a warp ranks one
+//                    32-point slice of an interval of up to 8192 points by
+//                    counting (rank = number of smaller values in the whole
+//                    interval), so the slices of a long interval run on many
+//                    warps at once; beyond 8192 points a CTA rebuilds the run
+//                    by scanning the frustum in order for that cell.
 //
 // The result is independent of the order the atomics happened in: counts
 // are exact and step 6 puts every interval in ascending p.  No kernel waits
@@ -41,21 +42,17 @@ constexpr int kTile = kThreads * kItems;        // 4096 frustum points per CTA t
 constexpr int kCellItems = 4;
 constexpr int kCellTile = kThreads * kCellItems; // 1024 cells per scan tile
 constexpr int kThreadSortMax = 16;              // longest interval one thread sorts in registers
-// Intervals of 65..128 points are ranked by one warp (four values a lane)
-// rather than sorted by a CTA in shared memory, and the list pass runs six
-// CTAs per SM (its residency) instead of four.  Measured, L2 flushed: Table-1
-// very large (2,377 such intervals) 101.6 -> 85.9 us, Table-1 large 49.1 ->
-// 47.4, canonical and BEVDet unchanged; a warp for up to 256 points was
-// slower (BEVDet 43.1 -> 52.2 us: eight values a lane).
-#ifndef BEVPOOL_MAP_WARP_SORT_MAX
-#define BEVPOOL_MAP_WARP_SORT_MAX 128
-#endif
+constexpr int kSliceSortMax = 8192;             // longest interval ranked in 32-point slices (at most 256 slices)
+static_assert(kCountingMaxCells <= (1 << 24), "a slice entry holds the interval index in 24 bits");
+// Slices replace a warp ranking a whole interval of up to 128 points and a
+// CTA sorting a longer one in shared memory (bitonic; a run of 464 points
+// held one CTA for 12 us, the end of the list pass).  Measured, map build
+// with L2 flushed: canonical 28.8 -> 26.8 us, BEVDet 42.5 -> 35.0, Table-1
+// large 47.9 -> 41.7, very large 86.2 -> 81.8, DRAM batch unchanged (no run
+// over 16 points).
 #ifndef BEVPOOL_MAP_LIST_CTAS_PER_SM
-#define BEVPOOL_MAP_LIST_CTAS_PER_SM 6
+#define BEVPOOL_MAP_LIST_CTAS_PER_SM 8           // the list pass's residency (32 registers, no shared buffer)
 #endif
-constexpr int kWarpSortMax = BEVPOOL_MAP_WARP_SORT_MAX;   // longest interval a warp ranks (a multiple of 32, <= 128)
-static_assert(kWarpSortMax % 32 == 0 && kWarpSortMax >= 64 && kWarpSortMax <= 128, "warp sorts hold 2..4 values a lane");
-constexpr int kCtaSortMax = 8192;               // longest interval sorted in shared memory
 
 struct CountWs {
     int32_t *count;       // [n_cells]  points per cell
@@ -65,9 +62,9 @@ struct CountWs {
     int32_t *tile_cnt;    // [cell tiles]
     int32_t *tile_nz;     // [cell tiles]
     int32_t *invalid;     // [1]
-    int32_t *lists;       // [2]: entries in mid_list, long_list
-    int32_t *mid_list;    // [min(n_frustum, n_cells)] intervals of 17..kWarpSortMax points
-    int32_t *long_list;   // [min(n_frustum, n_cells)] intervals of more than kWarpSortMax points
+    int32_t *lists;       // [2]: entries in slice_list, long_list
+    int32_t *slice_list;  // [n_frustum / 16 + 1] (interval << 8 | slice) of intervals of 17..kSliceSortMax points
+    int32_t *long_list;   // [min(n_frustum, n_cells)] intervals of more than kSliceSortMax points
 };
 
 size_t carve(void *base, int64_t nf, int32_t n_cells, CountWs *ws) {
@@ -88,7 +85,9 @@ size_t carve(void *base, int64_t nf, int32_t n_cells, CountWs *ws) {
     w.tile_nz = take(nct);
     w.invalid = take(1);
     w.lists = take(2);
-    w.mid_list = take(ni);
+    // an interval of L > 16 points has ceil(L / 32) <= L / 16 slices, so all
+    // of them together have at most n_frustum / 16
+    w.slice_list = take(nf / 16 + 1);
     w.long_list = take(ni);
     if (ws) *ws = w;
     return off;
@@ -250,61 +249,33 @@ struct Derive {
     }
 };
 
-// One warp ranks an interval of L <= 32*R points: each lane holds R values; a
-// value's rank is the number of smaller values (p are distinct).
-template <int R>
-__device__ __forceinline__ void warp_rank_sort(const int32_t *__restrict__ src, int s, int L, int cell,
-                                               const Derive &out) {
+// One warp ranks slice k of an interval [s, s + L) (its points s + 32k ..
+// s + 32k + 31): a value's rank is the number of smaller values in the whole
+// interval (p are distinct), counted over the interval 32 values at a time,
+// eight chunks of loads in flight.
+__device__ __forceinline__ void warp_rank_slice(const int32_t *__restrict__ src, int s, int L, int k, int cell,
+                                                const Derive &out) {
     const int lane = threadIdx.x & 31;
-    int v[R], rank[R];
+    const int idx = k * 32 + lane;
+    const int v = idx < L ? __ldg(src + s + idx) : INT_MAX;
+    const int nch = (L + 31) >> 5;                       // uniform over the warp
+    int rank = 0;
+    for (int c0 = 0; c0 < nch; c0 += 8) {
+        int x[8];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int idx = r * 32 + lane;
-        v[r] = idx < L ? __ldg(src + s + idx) : INT_MAX;
-        rank[r] = 0;
-    }
-#pragma unroll
-    for (int r2 = 0; r2 < R; ++r2) {
-        const int kmax = min(32, L - r2 * 32);                 // uniform over the warp
-#pragma unroll 4
-        for (int k = 0; k < kmax; ++k) {
-            const int x = __shfl_sync(0xffffffffu, v[r2], k);
-#pragma unroll
-            for (int r = 0; r < R; ++r) rank[r] += x < v[r];
+        for (int u = 0; u < 8; ++u) {
+            const int e = (c0 + u) * 32 + lane;
+            x[u] = e < L ? __ldg(src + s + e) : INT_MAX;
         }
-    }
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int idx = r * 32 + lane;
-        if (idx < L) out.put(s + rank[r], v[r], cell);
-    }
-}
-
-// The CTA sorts an interval of kWarpSortMax < L <= 8192 points in shared memory.
-__device__ __forceinline__ void cta_bitonic_sort(const int32_t *__restrict__ src, int s, int L, int cell,
-                                                 const Derive &out, int *buf) {
-    int n2 = 1;
-    while (n2 < L) n2 <<= 1;
-    for (int i = threadIdx.x; i < n2; i += kThreads) buf[i] = i < L ? __ldg(src + s + i) : INT_MAX;
-    __syncthreads();
-    for (int k = 2; k <= n2; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = threadIdx.x; i < n2; i += kThreads) {
-                const int ixj = i ^ j;
-                if (ixj > i) {
-                    const int a = buf[i], b = buf[ixj];
-                    const bool up = (i & k) == 0;
-                    if ((a > b) == up) {
-                        buf[i] = b;
-                        buf[ixj] = a;
-                    }
-                }
+        for (int u = 0; u < 8; ++u) {
+            if (c0 + u < nch) {                          // uniform
+#pragma unroll
+                for (int t = 0; t < 32; ++t) rank += __shfl_sync(0xffffffffu, x[u], t) < v;
             }
-            __syncthreads();
         }
     }
-    for (int i = threadIdx.x; i < L; i += kThreads) out.put(s + i, buf[i], cell);
-    __syncthreads();
+    if (idx < L) out.put(s + rank, v, cell);
 }
 
 // Longer intervals: rebuild the run in frustum order by a stable compaction of
@@ -362,7 +333,7 @@ __device__ __forceinline__ void thread_sort(const int32_t *__restrict__ src, int
 __global__ void __launch_bounds__(kThreads)
 k_sort_runs(const int32_t *__restrict__ tmp_p, const int32_t *__restrict__ starts,
             const int32_t *__restrict__ lengths, const int32_t *__restrict__ icell,
-            const int32_t *__restrict__ d_counts, int32_t *__restrict__ lists, int32_t *__restrict__ mid_list,
+            const int32_t *__restrict__ d_counts, int32_t *__restrict__ lists, int32_t *__restrict__ slice_list,
             int32_t *__restrict__ long_list, Derive out) {
     grid_dep_wait();
     grid_dep_allow();
@@ -376,43 +347,37 @@ k_sort_runs(const int32_t *__restrict__ tmp_p, const int32_t *__restrict__ start
         thread_sort<8>(tmp_p, s, L, cell, out);
     else if (L <= kThreadSortMax)
         thread_sort<kThreadSortMax>(tmp_p, s, L, cell, out);
-    else if (L <= kWarpSortMax)
-        mid_list[atomicAdd(lists + 0, 1)] = i;
-    else
+    else if (L <= kSliceSortMax) {
+        const int nsl = (L + 31) >> 5;
+        const int base = atomicAdd(lists + 0, nsl);
+        for (int k = 0; k < nsl; ++k) slice_list[base + k] = static_cast<int32_t>((static_cast<uint32_t>(i) << 8) | k);
+    } else {
         long_list[atomicAdd(lists + 1, 1)] = i;
+    }
 }
 
-// Persistent CTAs drain the lists: each warp ranks mid-list intervals, then
-// each CTA sorts long-list intervals in shared memory.
+// Persistent CTAs drain the lists: each warp ranks slices (32 points of an
+// interval of 17..kSliceSortMax points, so a long interval is spread over
+// many warps), then each CTA rebuilds the rare longer intervals by scanning
+// the frustum.
 __global__ void __launch_bounds__(kThreads)
 k_sort_lists(const int32_t *__restrict__ tmp_p, const int32_t *__restrict__ starts,
              const int32_t *__restrict__ lengths, const int32_t *__restrict__ icell,
-             const int32_t *__restrict__ lists, const int32_t *__restrict__ mid_list,
+             const int32_t *__restrict__ lists, const int32_t *__restrict__ slice_list,
              const int32_t *__restrict__ long_list, const int32_t *__restrict__ cell_ids, int64_t nf, Derive out) {
     grid_dep_wait();
     grid_dep_allow();
-    __shared__ int buf[kCtaSortMax];
     __shared__ int scratch[kWarps + 1];
-    const int n_mid = __ldg(lists + 0), n_long = __ldg(lists + 1);
+    const int n_slices = __ldg(lists + 0), n_long = __ldg(lists + 1);
     const int warps_total = gridDim.x * kWarps;
-    for (int x = blockIdx.x * kWarps + (threadIdx.x >> 5); x < n_mid; x += warps_total) {   // warp-uniform
-        const int j = __ldg(mid_list + x);
-        const int L = __ldg(lengths + j);
-        const int s = __ldg(starts + j), cell = __ldg(icell + j);
-        if (L <= 32)
-            warp_rank_sort<1>(tmp_p, s, L, cell, out);
-        else if (L <= 64)
-            warp_rank_sort<2>(tmp_p, s, L, cell, out);
-        else
-            warp_rank_sort<4>(tmp_p, s, L, cell, out);
+    for (int x = blockIdx.x * kWarps + (threadIdx.x >> 5); x < n_slices; x += warps_total) {   // warp-uniform
+        const uint32_t e = static_cast<uint32_t>(__ldg(slice_list + x));
+        const int j = static_cast<int>(e >> 8), k = static_cast<int>(e & 255u);
+        warp_rank_slice(tmp_p, __ldg(starts + j), __ldg(lengths + j), k, __ldg(icell + j), out);
     }
-    for (int x = blockIdx.x; x < n_long; x += gridDim.x) {                                // CTA-uniform
+    for (int x = blockIdx.x; x < n_long; x += gridDim.x) {                                   // CTA-uniform
         const int j = __ldg(long_list + x);
-        const int s = __ldg(starts + j), L = __ldg(lengths + j), cell = __ldg(icell + j);
-        if (L <= kCtaSortMax)
-            cta_bitonic_sort(tmp_p, s, L, cell, out, buf);
-        else
-            cta_scan_frustum(cell_ids, nf, s, cell, out, scratch);
+        cta_scan_frustum(cell_ids, nf, __ldg(starts + j), __ldg(icell + j), out, scratch);
     }
 }
 
@@ -460,11 +425,11 @@ cudaError_t launch_build_map_counting(const BuildMapArgs &a) {
     if (e == cudaSuccess)
         e = launch_dependent(k_sort_runs, dim3(static_cast<unsigned>(div_up(max_int, kThreads))), dim3(kThreads), 0,
                              st, ws.tmp_p, a.interval_starts, a.interval_lengths, ws.icell, a.d_counts, ws.lists,
-                             ws.mid_list, ws.long_list, out);
+                             ws.slice_list, ws.long_list, out);
     count_launch();
     if (e == cudaSuccess)
         e = launch_dependent(k_sort_lists, dim3(info.sm_count * BEVPOOL_MAP_LIST_CTAS_PER_SM), dim3(kThreads), 0, st, ws.tmp_p,
-                             a.interval_starts, a.interval_lengths, ws.icell, ws.lists, ws.mid_list, ws.long_list,
+                             a.interval_starts, a.interval_lengths, ws.icell, ws.lists, ws.slice_list, ws.long_list,
                              a.cell_ids, nf, out);
     count_launch();
     if (e != cudaSuccess) return e;
