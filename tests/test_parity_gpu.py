@@ -167,6 +167,29 @@ def test_edge_one_interval_of_20000_points(bp):
     _edge(bp, np.full(NC * D * H * W, 5), NC, D, H, W, 80, 9, "long_interval")
 
 
+def test_edge_run_lengths_at_sort_boundaries(bp):
+    """Runs whose lengths sit on either side of every sort boundary of the
+    map build: 16 / 17 points (one thread's registers / a warp's slice),
+    32 / 33 (one slice / two), 8192 / 8193 (256 slices / the frustum scan),
+    placed at random frustum positions so the order inside each run is
+    checked against the oracle's (cell, p) order."""
+    NC, D, H, W = 2, 30, 20, 25                       # 30,000 frustum points
+    nf = NC * D * H * W
+    lengths = [16, 17, 32, 33, 64, 65, 128, 129, 8191, 8192, 8193]
+    rng = np.random.default_rng(31)
+    cid = np.full(nf, -1, np.int64)
+    pos = rng.permutation(nf)
+    at = 0
+    for cell, L in enumerate(lengths):
+        cid[pos[at:at + L]] = cell
+        at += L
+    rest = pos[at:]
+    cid[rest] = np.where(rng.random(rest.size) < 0.5, rng.integers(len(lengths), 400, rest.size), -1)
+    m, _ = _edge(bp, cid, NC, D, H, W, 64, 400, "sort_boundaries")
+    got = np.bincount(m.ranks_bev[:m.n_points].cpu().numpy(), minlength=400)[:len(lengths)]
+    assert got.tolist() == lengths
+
+
 def test_edge_every_cell_hit_once(bp):
     NC, D, H, W = 2, 1, 16, 32
     nf = NC * D * H * W
