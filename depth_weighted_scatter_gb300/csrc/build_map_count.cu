@@ -328,7 +328,7 @@ __device__ __forceinline__ void thread_sort(const int32_t *__restrict__ src, int
 }
 
 // One thread per interval: intervals of up to kThreadSortMax points are
-// sorted in registers on the spot; longer ones are appended to the mid or
+// sorted in registers on the spot; longer ones are appended to the slice or
 // long work list for k_sort_lists (the list order does not affect the result).
 __global__ void __launch_bounds__(kThreads)
 k_sort_runs(const int32_t *__restrict__ tmp_p, const int32_t *__restrict__ starts,
