@@ -54,6 +54,31 @@ def test_nvfp4_every_channel_count(bp, C):
     assert_forward_close(wl, out, oracle_forward(wl))
 
 
+@pytest.mark.parametrize("intervals", ["short", "long"])
+@pytest.mark.parametrize("C", [64, 256])
+def test_nvfp4_streaming_regime(bp, C, intervals):
+    """A grid whose fp16 output (> 72 MiB) streams past the L2: the NVFP4
+    kernel with evict-first stores, fill CTAs after the first wave of compute
+    CTAs, every row checked (the few occupied ones and the many zeros)."""
+    cells = (72 << 20) // (2 * C) + 1
+    NC, D, H, W = 2, 11, 9, 13
+    rng = np.random.default_rng(C + 5 + 1000 * (intervals == "long"))
+    nf = NC * D * H * W
+    cid = rng.integers(0, cells, nf).astype(np.int32)
+    hot = rng.random(nf) < (0.3 if intervals == "short" else 0.97)
+    cid[hot] = rng.integers(0, 50, int(hot.sum()))      # a dense corner with long intervals
+    cid[rng.random(nf) < 0.2] = -1
+    wl = workloads._to_nvfp4(workloads.custom(NC, D, H, W, C, cells, cid, seed=C + 9), f"stream_C{C}_nvfp4_{intervals}")
+    plan = bp.forward_plan(bp.BEVPOOL_NVFP4, C, *wl.dims(), wl.n_kept, 1, cells)
+    assert plan["streaming"] == 1
+    cells_d, depth, feat = upload(wl)
+    m = bp.build_map(cells_d, *wl.dims(), wl.n_cells)
+    out = torch.full((cells, C), float("nan"), dtype=torch.float16, device="cuda")
+    gpu_forward(wl, m, depth, feat, out=out)
+    torch.cuda.synchronize()
+    assert_forward_close(wl, out, oracle_forward(wl))
+
+
 @pytest.mark.parametrize("name", ["canonical_nvfp4", "wide_c256_nvfp4"])
 def test_nvfp4_e4m3_out(bp, name, wl_cache):
     """NVFP4 features with depth and output in FP8, as in the pages' experiment."""

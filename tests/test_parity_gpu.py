@@ -196,6 +196,39 @@ def test_edge_every_cell_hit_once(bp):
     _edge(bp, np.random.default_rng(4).permutation(nf), NC, D, H, W, 64, nf, "bijection")
 
 
+def test_edge_largest_output(bp):
+    """n_cells * C just under 2^31 (the largest output the forward accepts, a
+    4 GB fp16 grid): points in the first and in the last cells, so rows at the
+    far end of the output (byte offsets near 4 GiB) are written and checked.
+    The expected rows come from the oracle run on the same points with the
+    occupied cells numbered compactly; every other row must be zero."""
+    from depth_weighted_scatter_gb300 import workloads
+
+    C = 256
+    cells = (2 ** 31 - 1) // C
+    NC, D, H, W = 1, 8, 8, 16
+    nf = NC * D * H * W
+    rng = np.random.default_rng(41)
+    cid = np.where(rng.random(nf) < 0.5, rng.integers(0, 60, nf), rng.integers(cells - 60, cells, nf))
+    cid[rng.random(nf) < 0.2] = -1
+    wl = workloads.custom(NC, D, H, W, C, cells, cid.astype(np.int32), seed=41, name="largest_output")
+    c_d, depth, feat = upload(wl)
+    m = _gpu_map(bp, wl, c_d)
+    _check_map(bp, wl, m)
+    out = torch.full((cells, C), float("nan"), dtype=torch.float16, device="cuda")
+    gpu_forward(wl, m, depth, feat, out=out)
+    torch.cuda.synchronize()
+    used = np.unique(cid[cid >= 0])
+    compact = np.where(cid >= 0, np.searchsorted(used, cid), -1).astype(np.int32)
+    wl_c = workloads.custom(NC, D, H, W, C, len(used), compact, name="largest_output_compact", depth=wl.depth,
+                            feat=wl.feat)
+    assert_forward_close(wl_c, out[torch.from_numpy(used).cuda()], oracle_forward(wl_c))
+    assert not bool(torch.isnan(out).any())
+    rows_nonzero = int((out != 0).any(dim=1).sum())
+    assert rows_nonzero <= len(used)
+    assert used.max() >= cells - 60                    # the far end of the grid is among the checked rows
+
+
 def test_edge_ragged_tiles_and_many_cells(bp):
     """Frustum not a multiple of the 4096-point tile; cell ids need 31 bits (3 radix passes)."""
     NC, D, H, W = 1, 37, 13, 11                       # 5291 points: one full tile + a ragged one
