@@ -185,3 +185,13 @@ def test_probe_l2_rejects_bad_arguments(bp):
     assert bp.bevpool_probe_l2(0, fake, 64, 0, fake, 0) == bp.BEVPOOL_ERR_INVALID_ARG     # no pass
     assert bp.bevpool_probe_l2(0, fake, 64, 1, 0, 0) == bp.BEVPOOL_ERR_INVALID_ARG        # read without sink
     assert bp.bevpool_probe_l2(1, fake, (1 << 32) + 16, 1, 0, 0) == bp.BEVPOOL_ERR_INVALID_ARG   # too large
+
+
+def test_probe_gather_rejects_bad_arguments(bp):
+    """Argument checks come before any CUDA call."""
+    fake = 1 << 20   # never dereferenced: every call below fails its checks first
+    good = dict(feat=fake, n_rows=100, row_bytes=160, rows=fake, n_points=1000, ctas_per_sm=3, d_sink=0, stream=0)
+    for change in [dict(feat=0), dict(feat=fake + 8), dict(n_rows=0), dict(row_bytes=8), dict(row_bytes=520),
+                   dict(row_bytes=40), dict(n_points=-1), dict(rows=0), dict(rows=fake + 2), dict(ctas_per_sm=0),
+                   dict(ctas_per_sm=9)]:
+        assert bp.bevpool_probe_gather(**{**good, **change}) == bp.BEVPOOL_ERR_INVALID_ARG, change
