@@ -179,16 +179,10 @@ k_offsets(const int32_t *__restrict__ count, int32_t n_cells, const int32_t *__r
           int32_t *__restrict__ d_counts) {
     grid_dep_wait();
     grid_dep_allow();
-    __shared__ long long red[kWarps];
-    __shared__ int scratch[kWarps + 1];
     const int b = blockIdx.x;
     long long pre = 0;
     for (int i = threadIdx.x; i < b; i += kThreads)
         pre += static_cast<long long>(tile_cnt[i]) + (static_cast<long long>(tile_nz[i]) << 32);
-    pre = cta_sum_ll(pre, red);
-    const int pre_cnt = static_cast<int>(pre & 0xffffffffll);
-    const int pre_nz = static_cast<int>(pre >> 32);
-
     const int64_t c0 = static_cast<int64_t>(b) * kCellTile + static_cast<int64_t>(threadIdx.x) * kCellItems;
     int v[kCellItems];
     int my_cnt = 0, my_nz = 0;
@@ -198,9 +192,37 @@ k_offsets(const int32_t *__restrict__ count, int32_t n_cells, const int32_t *__r
         my_cnt += v[j];
         my_nz += v[j] > 0;
     }
-    int tot_cnt, tot_nz;
-    int run_cnt = cta_exclusive_sum(my_cnt, scratch, &tot_cnt) + pre_cnt;
-    int run_nz = cta_exclusive_sum(my_nz, scratch, &tot_nz) + pre_nz;
+    // One scan for both running sums and the sum of the earlier tiles: points
+    // in the low 32 bits, non-empty cells in the high 32 (every sum < 2^31,
+    // so nothing carries between the halves), one barrier.
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long my = static_cast<long long>(my_cnt) + (static_cast<long long>(my_nz) << 32);
+    long long x = my;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) pre += __shfl_xor_sync(0xffffffffu, pre, o);
+    __shared__ long long s_scan[kWarps], s_pre[kWarps];
+    if (lane == 31) s_scan[warp] = x;
+    if (lane == 0) s_pre[warp] = pre;
+    __syncthreads();
+    long long base = 0, tot = 0, pre_all = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const long long t = s_scan[w];
+        if (w < warp) base += t;
+        tot += t;
+        pre_all += s_pre[w];
+    }
+    const int pre_cnt = static_cast<int>(pre_all & 0xffffffffll);
+    const int pre_nz = static_cast<int>(pre_all >> 32);
+    const long long ex = base + x - my;
+    int run_cnt = static_cast<int>(ex & 0xffffffffll) + pre_cnt;
+    int run_nz = static_cast<int>(ex >> 32) + pre_nz;
+    const int tot_cnt = static_cast<int>(tot & 0xffffffffll), tot_nz = static_cast<int>(tot >> 32);
 #pragma unroll
     for (int j = 0; j < kCellItems; ++j) {
         if (c0 + j < n_cells) {
